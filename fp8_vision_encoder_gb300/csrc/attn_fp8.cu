@@ -1,0 +1,564 @@
+// FP8 variable-length non-causal attention on 5th-generation tensor cores.
+//
+// "FP8 ViT Encoder Attention", intro: Q/K/V are quantized to FP8 before the
+// attention call; Performance: the FP8 attention kernel at head_dim 128,
+// seq_len 8192.  "FP8 vision encoder attention" (Sonar), Requirements: packed
+// variable-length image batches with per-tensor FP8 scales.
+//
+// One CTA computes 2 query tiles of 128 rows (256 consecutive queries of one
+// segment and head) against every key tile of that segment:
+//
+//   warp 8      TMA producer: Q tiles once, then K and V^T tiles through a
+//               3-stage shared-memory ring (128-byte swizzle).
+//   warp 9      MMA issuer (one thread): S_w = Q_w K^T and O_w += P_w V into
+//               tensor memory, tcgen05.mma kind::f8f6f4 (E4M3 x E4M3 -> F32).
+//   warps 0-3   softmax for query tile 0, warps 4-7 for query tile 1: one
+//               thread per query row, reading its S row from TMEM.
+//
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.
+//
+// Softmax in log2 units: x = S_raw * c, c = scale_q scale_k sm_scale log2(e).
+// Each row keeps an integer reference m_ref; P' = E4M3(2^(x - m_ref + 4)).
+// O and l are rescaled (by an exact power of two) only when a tile's max
+// exceeds m_ref + 4, which keeps P' <= 256 < 448 (no saturation) and makes the
+// E4M3 rounding of P independent of the reference chosen.  l sums the
+// unrounded fp32 values.  o = O * scale_v / l, rounded to bf16.
+//
+// Keys are walked in tiles starting at floor16(segment start) so that every
+// V^T tile starts at a 16-byte-aligned token coordinate; keys outside the
+// segment are masked to -inf (only the first and last tile need it).
+//
+// Every wait on an mbarrier is bounded; on expiry the CTA records
+// VITFP8_ERR_DEVICE_TIMEOUT in the workspace error word, all roles leave their
+// loops, wait (bounded) for their own async work, free TMEM and return.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace vitfp8 {
+
+namespace fa {
+constexpr int BM = 128;                  // query rows per tile
+constexpr int NQT = 2;                   // query tiles per CTA
+constexpr int ROWS_PER_ITEM = BM * NQT;  // queries per work item
+constexpr int BN = 128;                  // keys per tile
+constexpr int NST = 3;                   // K/V pipeline stages
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr int TILE = 128 * 128;          // bytes of one 128-row x 128-byte tile
+constexpr int HEADROOM = 4;              // rescale when max grows past m_ref + HEADROOM
+constexpr float PSHIFT = 8 - HEADROOM;   // P' = 2^(x - m_ref + PSHIFT) <= 2^8
+
+constexpr int SM_Q = 0;
+constexpr int SM_K = SM_Q + NQT * TILE;
+constexpr int SM_V = SM_K + NST * TILE;
+constexpr int SM_P = SM_V + NST * TILE;
+constexpr int SM_BAR = SM_P + NQT * TILE;
+// barrier indices
+constexpr int B_QFULL = 0;
+constexpr int B_KFULL = 1;
+constexpr int B_VFULL = B_KFULL + NST;
+constexpr int B_KVEMPTY = B_VFULL + NST;
+constexpr int B_SFULL = B_KVEMPTY + NST;   // [NQT]
+constexpr int B_SFREE = B_SFULL + NQT;     // [NQT]
+constexpr int B_PFULL = B_SFREE + NQT;     // [NQT]
+constexpr int B_PVDONE = B_PFULL + NQT;    // [NQT]
+constexpr int B_FINAL = B_PVDONE + NQT;
+constexpr int NBAR = B_FINAL + 1;
+constexpr int SM_TMEMPTR = SM_BAR + NBAR * 8;
+constexpr int SM_ABORT = SM_TMEMPTR + 4;
+constexpr int SM_USED = SM_ABORT + 4;
+constexpr int SMEM_BYTES = SM_USED + 1024;  // + slack to align the base to 1024
+constexpr uint32_t TMEM_COLS = 512;
+constexpr long long WAIT_LIMIT = 1000000000LL;  // cycles (~0.5 s) before a wait gives up
+}  // namespace fa
+
+struct AttnParams {
+    const int32_t* cu;
+    const int32_t* order;
+    const int32_t* prefix;
+    WsHeader* ws;
+    const vitfp8_scale_state* st;
+    uint16_t* out;
+    int nseq, T, H, D, DV, KS;
+    float sm_scale;
+};
+
+// Bounded wait: true when the phase with `parity` completed; false if the CTA
+// aborted or this wait timed out (which sets the abort flag and the error).
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      int32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > fa::WAIT_LIMIT) {
+                *abort_flag = 1;
+                record_error(err, VITFP8_ERR_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]));
+}
+
+// 2^k for an integer-valued float k in [-126, 0].
+__device__ __forceinline__ float exp2_int(float k) {
+    int e = int(k) + 127;
+    e = e < 1 ? 1 : e;
+    return __int_as_float(e << 23);
+}
+
+__global__ void __launch_bounds__(fa::NUM_THREADS, 1)
+attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using namespace fa;
+    const int item = blockIdx.x;
+    const int total = p.ws->total_items;
+    if (item >= total) return;
+
+    // ---- work item -> (segment, head, query tile pair)
+    int lo = 0, hi = p.nseq - 1;  // largest pos with prefix[pos] <= item
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.prefix[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    const int b = p.order[lo];
+    const int local = item - p.prefix[lo];
+    const int seg_s = p.cu[b];
+    const int seg_e = p.cu[b + 1];
+    const int L = seg_e - seg_s;
+    const int nq = (L + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
+    const int h = local / nq;
+    const int qt = local - h * nq;
+    const int q0 = seg_s + qt * ROWS_PER_ITEM;
+    const int kbase = seg_s & ~15;
+    const int nkv = (seg_e - kbase + BN - 1) / BN;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
+    int32_t* err = &p.ws->error;
+    auto BAR = [&](int i) -> uint32_t { return sb + SM_BAR + 8u * uint32_t(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_QFULL), 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(BAR(B_KFULL + s), 1);
+            mbar_init(BAR(B_VFULL + s), 1);
+            mbar_init(BAR(B_KVEMPTY + s), 1);
+        }
+        for (int w = 0; w < NQT; ++w) {
+            mbar_init(BAR(B_SFULL + w), 1);
+            mbar_init(BAR(B_SFREE + w), 4);
+            mbar_init(BAR(B_PFULL + w), 4);
+            mbar_init(BAR(B_PVDONE + w), 1);
+        }
+        mbar_init(BAR(B_FINAL), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(sb + SM_TMEMPTR, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEMPTR);
+
+    if (warp == WARP_TMA) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(BAR(B_QFULL), NQT * TILE);
+            for (int w = 0; w < NQT; ++w)
+                tma_load_3d(sb + SM_Q + w * TILE, &tmQ, BAR(B_QFULL), 0, h, q0 + w * BM);
+            const uint32_t vbytes = uint32_t(p.DV) * 128u;
+            int j = 0;
+            for (; j < nkv; ++j) {
+                const int s = j % NST;
+                if (j >= NST && !bwait(BAR(B_KVEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
+                const int key0 = kbase + j * BN;
+                mbar_arrive_expect_tx(BAR(B_KFULL + s), TILE);
+                tma_load_3d(sb + SM_K + s * TILE, &tmK, BAR(B_KFULL + s), 0, h, key0);
+                mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
+                tma_load_3d(sb + SM_V + s * TILE, &tmV, BAR(B_VFULL + s), key0, 0, h);
+            }
+            if (*abort_flag) {
+                // Let the copies this thread started land before the CTA exits.
+                bwait(BAR(B_QFULL), 0, abort_flag, err);
+                for (int jj = (j > NST ? j - NST : 0); jj < j; ++jj) {
+                    const int s = jj % NST;
+                    const uint32_t ph = (jj / NST) & 1;
+                    for (int spin = 0; spin < (1 << 22); ++spin)
+                        if (mbar_try_wait(BAR(B_KFULL + s), ph)) break;
+                    for (int spin = 0; spin < (1 << 22); ++spin)
+                        if (mbar_try_wait(BAR(B_VFULL + s), ph)) break;
+                }
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = make_idesc(0, BM, BN);
+            const uint32_t idPV = make_idesc(0, BM, p.DV);
+            auto issue_S = [&](int w, int s) {
+                tc_fence_after();
+                for (int kk = 0; kk < p.KS; ++kk)
+                    umma_f8(tmem + uint32_t(w * BN),
+                            sw128_kmajor_desc(sb + SM_Q + w * TILE + kk * 32),
+                            sw128_kmajor_desc(sb + SM_K + s * TILE + kk * 32), idS, kk > 0);
+                tc_commit(BAR(B_SFULL + w));
+            };
+            auto issue_PV = [&](int w, int s, bool acc) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BN / 32; ++kk)
+                    umma_f8(tmem + uint32_t(2 * BN + w * BN),
+                            sw128_kmajor_desc(sb + SM_P + w * TILE + kk * 32),
+                            sw128_kmajor_desc(sb + SM_V + s * TILE + kk * 32), idPV,
+                            (acc || kk > 0) ? 1u : 0u);
+                tc_commit(BAR(B_PVDONE + w));
+            };
+            bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
+                      bwait(BAR(B_KFULL + 0), 0, abort_flag, err);
+            if (ok) {
+                issue_S(0, 0);
+                issue_S(1, 0);
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int s = j % NST;
+                const uint32_t ph = (j / NST) & 1;
+                const bool nxt = j + 1 < nkv;
+                const int s1 = (j + 1) % NST;
+                const uint32_t ph1 = ((j + 1) / NST) & 1;
+                if (nxt) {
+                    ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err) &&
+                         bwait(BAR(B_SFREE + 0), j & 1, abort_flag, err);
+                    if (!ok) break;
+                    issue_S(0, s1);
+                }
+                ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err) &&
+                     bwait(BAR(B_PFULL + 0), j & 1, abort_flag, err);
+                if (!ok) break;
+                issue_PV(0, s, j > 0);
+                if (nxt) {
+                    ok = bwait(BAR(B_SFREE + 1), j & 1, abort_flag, err);
+                    if (!ok) break;
+                    issue_S(1, s1);
+                }
+                ok = bwait(BAR(B_PFULL + 1), j & 1, abort_flag, err);
+                if (!ok) break;
+                issue_PV(1, s, j > 0);
+                tc_commit(BAR(B_KVEMPTY + s));
+            }
+            // Every MMA issued above has completed before TMEM is released.
+            tc_commit(BAR(B_FINAL));
+            for (int spin = 0; spin < (1 << 24); ++spin)
+                if (mbar_try_wait(BAR(B_FINAL), 0)) break;
+        }
+    } else {
+        // ------------------------------------------------ softmax (warps 0..7)
+        const int w = warp >> 2;              // query tile
+        const int sub = warp & 3;             // TMEM lane quarter
+        const int r = sub * 32 + lane;        // row inside the query tile
+        const int qrow = q0 + w * BM + r;     // packed token index of this row
+        const bool row_valid = qrow < seg_e;
+        const uint32_t lane_off = uint32_t(sub * 32) << 16;
+        const uint32_t tS = tmem + lane_off + uint32_t(w * BN);
+        const uint32_t tO = tmem + lane_off + uint32_t(2 * BN + w * BN);
+        const float c = p.st->scale[0] * p.st->scale[1] * p.sm_scale * 1.4426950408889634f;
+        uint8_t* prow = smem + SM_P + w * TILE + (r >> 3) * 1024 + (r & 7) * 128;
+        float m_ref = 0.0f;
+        float l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + w), j & 1, abort_flag, err));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t s0[32], s1[32], s2[32], s3[32];
+            tmem_ld_32x32b_x32(tS + 0, s0);
+            tmem_ld_32x32b_x32(tS + 32, s1);
+            tmem_ld_32x32b_x32(tS + 64, s2);
+            tmem_ld_32x32b_x32(tS + 96, s3);
+            tmem_ld_wait(s0);
+            reg_fence32(s1);
+            reg_fence32(s2);
+            reg_fence32(s3);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SFREE + w));
+
+            float sf[128];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                sf[i] = __uint_as_float(s0[i]);
+                sf[32 + i] = __uint_as_float(s1[i]);
+                sf[64 + i] = __uint_as_float(s2[i]);
+                sf[96 + i] = __uint_as_float(s3[i]);
+            }
+            const int key0 = kbase + j * BN;
+            if (key0 < seg_s || key0 + BN > seg_e) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    const int key = key0 + i;
+                    if (key < seg_s || key >= seg_e) sf[i] = -INFINITY;
+                }
+            }
+            float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
+#pragma unroll
+            for (int i = 4; i < 128; i += 4) {
+                mx0 = fmaxf(mx0, sf[i]);
+                mx1 = fmaxf(mx1, sf[i + 1]);
+                mx2 = fmaxf(mx2, sf[i + 2]);
+                mx3 = fmaxf(mx3, sf[i + 3]);
+            }
+            const float xmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+            float oscale = 1.0f;
+            bool need = false;
+            if (j == 0) {
+                m_ref = ceilf(xmax);
+            } else if (xmax > m_ref + float(HEADROOM)) {
+                const float mnew = ceilf(xmax);
+                oscale = exp2_int(m_ref - mnew);
+                l *= oscale;
+                m_ref = mnew;
+                need = true;
+            }
+            const float bias = PSHIFT - m_ref;
+            uint32_t pk[32];
+            float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float p0 = ex2_approx(fmaf(sf[4 * i + 0], c, bias));
+                const float p1 = ex2_approx(fmaf(sf[4 * i + 1], c, bias));
+                const float p2 = ex2_approx(fmaf(sf[4 * i + 2], c, bias));
+                const float p3 = ex2_approx(fmaf(sf[4 * i + 3], c, bias));
+                ls0 += p0 + p1;
+                ls1 += p2 + p3;
+                pk[i] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
+            }
+            l += ls0 + ls1;
+
+            if (j > 0) {
+                ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_PVDONE + w), (j - 1) & 1, abort_flag, err));
+                if (!ok) break;
+            }
+            if (__any_sync(0xFFFFFFFFu, need)) {
+                tc_fence_after();
+                for (int cc = 0; cc < p.DV; cc += 16) {
+                    uint32_t o[16];
+                    tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
+                    tmem_ld_wait16(o);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * oscale);
+                    tmem_st_32x32b_x16(tO + uint32_t(cc), o);
+                }
+                tmem_st_wait();
+            }
+            // P row -> shared memory, K-major with 128-byte swizzle.
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_PFULL + w));
+        }
+        if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_PVDONE + w), (nkv - 1) & 1, abort_flag, err));
+        if (ok) {
+            tc_fence_after();
+            const float oscale = p.st->scale[2] / l;
+            uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
+            for (int cc = 0; cc < p.DV; cc += 16) {
+                uint32_t o[16];
+                tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
+                tmem_ld_wait16(o);
+                uint32_t pkd[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(o[2 * q]) * oscale,
+                                                              __uint_as_float(o[2 * q + 1]) * oscale);
+                    pkd[q] = *reinterpret_cast<uint32_t*>(&v2);
+                }
+                if (row_valid) {
+                    if (cc + 8 <= p.D)
+                        *reinterpret_cast<uint4*>(orow + cc) = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+                    if (cc + 16 <= p.D)
+                        *reinterpret_cast<uint4*>(orow + cc + 8) = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+                }
+            }
+        }
+    }
+
+    // ---- teardown: all TMEM traffic of this CTA is complete past this barrier.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// Work list: segments sorted longest first (when there are at most 2048),
+// items per segment = ceil(L / 256) * H, prefix sums over the sorted order.
+__global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T, int H,
+                                 int rows_per_item, WsHeader* ws, int32_t* order, int32_t* prefix) {
+    __shared__ int bad;
+    if (threadIdx.x == 0) {
+        ws->error = 0;
+        bad = (cu[0] != 0 || cu[nseq] != T) ? 1 : 0;
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < nseq; b += blockDim.x)
+        if (cu[b + 1] < cu[b]) atomicOr(&bad, 1);
+    __syncthreads();
+    if (bad) {
+        if (threadIdx.x == 0) {
+            ws->total_items = 0;
+            ws->num_seqs = nseq;
+            record_error(&ws->error, VITFP8_ERR_BAD_SEQLENS);
+        }
+        return;
+    }
+    for (int b = threadIdx.x; b < nseq; b += blockDim.x) {
+        const int Lb = cu[b + 1] - cu[b];
+        int rank = b;
+        if (nseq <= 2048) {
+            rank = 0;
+            for (int b2 = 0; b2 < nseq; ++b2) {
+                const int L2 = cu[b2 + 1] - cu[b2];
+                rank += (L2 > Lb) || (L2 == Lb && b2 < b);
+            }
+        }
+        order[rank] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        prefix[0] = 0;
+        for (int i = 0; i < nseq; ++i) {
+            const int bb = order[i];
+            const int Lb = cu[bb + 1] - cu[bb];
+            acc += ((Lb + rows_per_item - 1) / rows_per_item) * H;
+            prefix[i + 1] = acc;
+        }
+        ws->total_items = acc;
+        ws->num_seqs = nseq;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+using EncodeFn = decltype(&cuTensorMapEncodeTiled);
+
+EncodeFn get_encode_fn() {
+    static EncodeFn fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(ptr);
+    }
+    return fn;
+}
+
+bool make_map_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1, stride2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
+                             void* ws, cudaStream_t s) {
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    int32_t* order = reinterpret_cast<int32_t*>(hdr + 1);
+    int32_t* prefix = order + nseq;
+    attn_plan_kernel<<<1, 1024, 0, s>>>(cu, nseq, T, H, rows_per_item, hdr, order, prefix);
+    return cudaGetLastError();
+}
+
+vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                              const vitfp8_scale_state* st, const int32_t* cu, int nseq, int T,
+                              int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,
+                              void* ws, cudaStream_t s) {
+    using namespace fa;
+    const int DV = (D + 15) & ~15;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_3d_u8(&mq, q8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
+                        uint64_t(H) * Dp, 128, 1, BM) ||
+        !make_map_3d_u8(&mk, k8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
+                        uint64_t(H) * Dp, 128, 1, BN) ||
+        !make_map_3d_u8(&mv, v8t, uint64_t(Tv), uint64_t(Dp), uint64_t(H), uint64_t(Tv),
+                        uint64_t(Tv) * Dp, BN, uint32_t(DV), 1))
+        return VITFP8_ERR_CUDA;
+
+    if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, ws, s) != cudaSuccess) return VITFP8_ERR_CUDA;
+
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess)
+            return VITFP8_ERR_CUDA;
+        attr_set = true;
+    }
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    AttnParams prm;
+    prm.cu = cu;
+    prm.order = reinterpret_cast<const int32_t*>(hdr + 1);
+    prm.prefix = prm.order + nseq;
+    prm.ws = hdr;
+    prm.st = st;
+    prm.out = out;
+    prm.nseq = nseq;
+    prm.T = T;
+    prm.H = H;
+    prm.D = D;
+    prm.DV = DV;
+    prm.KS = (D + 31) / 32;
+    prm.sm_scale = sm_scale;
+    const long long grid = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H;
+    if (grid > 0x7FFFFFFFLL) return VITFP8_ERR_UNSUPPORTED;
+    attn_fp8_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);
+    return cudaGetLastError() == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
+}
+
+}  // namespace vitfp8

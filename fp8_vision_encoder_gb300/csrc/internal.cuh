@@ -1,0 +1,57 @@
+// Internal declarations shared by the host API (api.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "vitfp8.h"
+
+namespace vitfp8 {
+
+// Source layout as passed to kernels (by value).
+struct SrcDev {
+    int32_t padded;
+    int64_t s_max;
+    int64_t ts;  // token stride, elements
+    int64_t hs;  // head stride, elements
+};
+
+// Attention workspace header (device), followed by int32 order[num_seqs] and
+// int32 prefix[num_seqs + 1].
+struct WsHeader {
+    int32_t error;        // first device-detected vitfp8_status
+    int32_t total_items;  // work items of the current call
+    int32_t num_seqs;
+    int32_t pad[13];
+};
+static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
+
+inline size_t ws_bytes(int32_t num_seqs) {
+    size_t b = sizeof(WsHeader) + sizeof(int32_t) * (2 * size_t(num_seqs) + 1);
+    return (b + 255) & ~size_t(255);
+}
+
+__device__ __forceinline__ void record_error(int32_t* word, int32_t code) {
+    atomicCAS(word, 0, code);
+}
+
+// ---- launchers (quant.cu)
+cudaError_t launch_state_init(vitfp8_scale_state* st, cudaStream_t s);
+cudaError_t launch_set_static(vitfp8_scale_state* st, float q, float k, float v, cudaStream_t s);
+cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
+                        const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
+                        int D, cudaStream_t s);
+cudaError_t launch_quant(const vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
+                         const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
+                         int D, int Dp, uint8_t* q8, uint8_t* k8, uint8_t* v8t, int64_t Tv,
+                         cudaStream_t s);
+
+// ---- launchers (attn_fp8.cu)
+cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
+                             void* ws, cudaStream_t s);
+vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                              const vitfp8_scale_state* st, const int32_t* cu, int nseq, int T,
+                              int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,
+                              void* ws, cudaStream_t s);
+
+}  // namespace vitfp8

@@ -1,0 +1,303 @@
+// Dynamic amax + 16-entry ring update, and quantize + un-pad of Q, K, V.
+//
+// "FP8 ViT Encoder Attention", Usage: a 16-entry circular buffer of observed
+// Q/K/V amax values drives per-forward scale updates; intro and note: Q/K/V are
+// quantized on the fly to FP8 before the attention call, with "quantization
+// kernel launches + un-padding".  Here both steps cover q, k and v in ONE
+// launch each (the pages cite three quantization launches plus un-padding).
+//
+// Both kernels are HBM-bound streams: 16-byte vector loads of 8 bf16 values,
+// coalesced along the head dim, tiles of 64 tokens x one head per block.
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace vitfp8 {
+
+constexpr int QT_TOK = 64;       // tokens per block tile
+constexpr int QT_THREADS = 256;  // threads per block
+constexpr int MAX_DP = 256;      // largest padded head dim the quant kernel takes
+
+// ---------------------------------------------------------------- helpers
+
+// Source row of packed token t (padded batch: b * s_max + i; packed: t), or -1
+// if cu_seqlens puts t outside its segment's padded rows.
+__device__ __forceinline__ int64_t src_row_of(const SrcDev& L, const int32_t* cu, int nseq, int t,
+                                              int32_t* err) {
+    if (!L.padded) return t;
+    int lo = 0, hi = nseq - 1;  // largest b with cu[b] <= t
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    int64_t i = int64_t(t) - __ldg(cu + lo);
+    if (i < 0 || i >= L.s_max) {
+        record_error(err, VITFP8_ERR_BAD_SEQLENS);
+        return -1;
+    }
+    return int64_t(lo) * L.s_max + i;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const uint16_t* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Running max of |x| over two bf16 lanes, as 16-bit magnitude patterns.  For
+// non-NaN values the magnitude bits order like the magnitudes; NaN patterns
+// (above 0x7F80) are dropped (fmax semantics), +inf (0x7F80) is kept.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m, uint32_t w) {
+    uint32_t a = w & 0x7FFF7FFFu;
+    uint32_t nan = __vcmpgtu2(a, 0x7F807F80u);
+    return __vmaxu2(m, a & ~nan);
+}
+
+// 4 bf16 (two words) -> 4 E4M3 codes of float32(x) * inv.
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float inv) {
+    float y0 = __fmul_rn(__uint_as_float(w0 << 16), inv);
+    float y1 = __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), inv);
+    float y2 = __fmul_rn(__uint_as_float(w1 << 16), inv);
+    float y3 = __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), inv);
+    return cvt_e4m3x2(y0, y1) | (cvt_e4m3x2(y2, y3) << 16);
+}
+
+__device__ __forceinline__ void scale_from_amax(float A, float& sc, float& inv) {
+    if (A == 0.0f) {
+        sc = 1.0f;
+        inv = 1.0f;
+    } else {
+        sc = __fdiv_rn(A, VITFP8_E4M3_MAX);
+        inv = __fdiv_rn(VITFP8_E4M3_MAX, A);
+    }
+}
+
+// ---------------------------------------------------------------- state
+
+__global__ void state_init_kernel(vitfp8_scale_state* st) {
+    for (int t = 0; t < 3; ++t) {
+        for (int i = 0; i < VITFP8_RING; ++i) st->hist[t][i] = 0.0f;
+        st->amax_ref[t] = 0.0f;
+        st->scale[t] = 1.0f;
+        st->inv_scale[t] = 1.0f;
+        st->amax_cur[t] = 0.0f;
+        st->amax_bits[t] = 0u;
+    }
+    st->pos = 0;
+    st->count = 0;
+    st->mode = 0;
+    st->dev_error = 0;
+    st->blocks_done = 0u;
+}
+
+__global__ void set_static_kernel(vitfp8_scale_state* st, float q, float k, float v) {
+    const float a[3] = {q, k, v};
+    st->mode = 1;
+    for (int t = 0; t < 3; ++t) {
+        st->amax_ref[t] = a[t];
+        scale_from_amax(a[t], st->scale[t], st->inv_scale[t]);
+    }
+}
+
+// ---------------------------------------------------------------- amax
+
+__global__ void __launch_bounds__(QT_THREADS)
+amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+            const uint16_t* __restrict__ v, SrcDev L, const int32_t* __restrict__ cu, int nseq,
+            int T, int H, int D) {
+    if (st->mode != 0) return;  // static mode: nothing to track
+    const int z = blockIdx.z;
+    const uint16_t* src = z == 0 ? q : (z == 1 ? k : v);
+    const int t0 = blockIdx.x * QT_TOK;
+    const int h = blockIdx.y;
+    __shared__ int64_t rows[QT_TOK];
+    __shared__ uint32_t wmax[QT_THREADS / 32];
+    if (threadIdx.x < QT_TOK) {
+        const int t = t0 + threadIdx.x;
+        rows[threadIdx.x] = t < T ? src_row_of(L, cu, nseq, t, &st->dev_error) : -1;
+    }
+    __syncthreads();
+
+    const int VD = D >> 3;
+    const int nvec = QT_TOK * VD;
+    const int64_t hoff = int64_t(h) * L.hs;
+    uint32_t m = 0;
+    for (int base = threadIdx.x; base < nvec; base += 4 * QT_THREADS) {
+        uint4 w[4];
+        bool ok[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * QT_THREADS;
+            const int tt = i / VD;
+            const int c = i - tt * VD;
+            ok[u] = i < nvec && rows[tt < QT_TOK ? tt : 0] >= 0;
+            w[u] = ok[u] ? ld_stream16(src + rows[tt] * L.ts + hoff + c * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            m = absmax_bf16x2(m, w[u].x);
+            m = absmax_bf16x2(m, w[u].y);
+            m = absmax_bf16x2(m, w[u].z);
+            m = absmax_bf16x2(m, w[u].w);
+        }
+    }
+    m = max(m & 0xFFFFu, m >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+
+    uint32_t bm = 0;
+#pragma unroll
+    for (int w = 0; w < QT_THREADS / 32; ++w) bm = max(bm, wmax[w]);
+    if (bm) atomicMax(&st->amax_bits[z], bm);
+    __threadfence();
+    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned prev = atomicAdd(&st->blocks_done, 1u);
+    if (prev != total - 1) return;
+
+    // Last block: every other block's atomicMax is visible.  Push-then-scale.
+    __threadfence();
+    const int pos = st->pos;
+    for (int t = 0; t < 3; ++t) {
+        const uint32_t bits = atomicExch(&st->amax_bits[t], 0u);
+        const float a = __uint_as_float(bits << 16);
+        st->amax_cur[t] = a;
+        st->hist[t][pos] = a;
+    }
+    st->pos = (pos + 1) % VITFP8_RING;
+    st->count = min(st->count + 1, VITFP8_RING);
+    for (int t = 0; t < 3; ++t) {
+        float A = 0.0f;
+        for (int i = 0; i < VITFP8_RING; ++i) A = fmaxf(A, st->hist[t][i]);
+        st->amax_ref[t] = A;
+        scale_from_amax(A, st->scale[t], st->inv_scale[t]);
+    }
+    st->blocks_done = 0u;
+}
+
+// ---------------------------------------------------------------- quantize
+
+__global__ void __launch_bounds__(QT_THREADS)
+quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restrict__ q,
+             const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, SrcDev L,
+             const int32_t* __restrict__ cu, int nseq, int T, int H, int D, int Dp,
+             uint8_t* __restrict__ q8, uint8_t* __restrict__ k8, uint8_t* __restrict__ v8t,
+             int64_t Tv, int32_t* err) {
+    const int z = blockIdx.z;
+    const uint16_t* src = z == 0 ? q : (z == 1 ? k : v);
+    const int t0 = blockIdx.x * QT_TOK;
+    const int h = blockIdx.y;
+    __shared__ int64_t rows[QT_TOK];
+    // V transpose tile: QT_TOK token rows of Dp code bytes, padded by one word
+    // per row to spread banks.
+    __shared__ uint32_t tile[QT_TOK * (MAX_DP / 4 + 1)];
+    if (threadIdx.x < QT_TOK) {
+        const int t = t0 + threadIdx.x;
+        rows[threadIdx.x] = t < T ? src_row_of(L, cu, nseq, t, err) : -1;
+    }
+    __syncthreads();
+
+    const float inv = st->inv_scale[z];
+    const int VD = D >> 3;   // source vectors per row
+    const int VP = Dp >> 3;  // output 8-byte groups per row
+    const int nvec = QT_TOK * VP;
+    const int64_t hoff = int64_t(h) * L.hs;
+    const int SW = Dp / 4 + 1;
+
+    for (int base = threadIdx.x; base < nvec; base += 4 * QT_THREADS) {
+        uint4 w[4];
+        bool ld[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * QT_THREADS;
+            const int tt = i / VP;
+            const int c = i - tt * VP;
+            ld[u] = i < nvec && c < VD && rows[tt < QT_TOK ? tt : 0] >= 0;
+            w[u] = ld[u] ? ld_stream16(src + rows[tt] * L.ts + hoff + c * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * QT_THREADS;
+            if (i >= nvec) continue;
+            const int tt = i / VP;
+            const int c = i - tt * VP;
+            uint2 o = make_uint2(0u, 0u);
+            if (ld[u]) {
+                o.x = quant4(w[u].x, w[u].y, inv);
+                o.y = quant4(w[u].z, w[u].w, inv);
+            }
+            if (z < 2) {
+                const int t = t0 + tt;
+                if (t < T) {
+                    uint8_t* dst = (z == 0 ? q8 : k8) + (int64_t(t) * H + h) * Dp + c * 8;
+                    *reinterpret_cast<uint2*>(dst) = o;
+                }
+            } else {
+                tile[tt * SW + 2 * c] = o.x;
+                tile[tt * SW + 2 * c + 1] = o.y;
+            }
+        }
+    }
+    if (z < 2) return;
+
+    // V: write [h][d][t] rows of 4 tokens x 4 d at a time (4x4 byte transpose).
+    __syncthreads();
+    const int nq = (Dp / 4) * (QT_TOK / 4);
+    for (int i = threadIdx.x; i < nq; i += QT_THREADS) {
+        const int tq = i % (QT_TOK / 4);
+        const int dq = i / (QT_TOK / 4);
+        const int tt = tq * 4;
+        const int64_t t = int64_t(t0) + tt;
+        if (t >= Tv) continue;
+        const uint32_t w0 = tile[(tt + 0) * SW + dq];
+        const uint32_t w1 = tile[(tt + 1) * SW + dq];
+        const uint32_t w2 = tile[(tt + 2) * SW + dq];
+        const uint32_t w3 = tile[(tt + 3) * SW + dq];
+        const uint32_t a0 = __byte_perm(w0, w1, 0x5140);
+        const uint32_t a1 = __byte_perm(w2, w3, 0x5140);
+        const uint32_t a2 = __byte_perm(w0, w1, 0x7362);
+        const uint32_t a3 = __byte_perm(w2, w3, 0x7362);
+        const uint32_t o[4] = {__byte_perm(a0, a1, 0x5410), __byte_perm(a0, a1, 0x7632),
+                               __byte_perm(a2, a3, 0x5410), __byte_perm(a2, a3, 0x7632)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint32_t*>(v8t + (int64_t(h) * Dp + dq * 4 + j) * Tv + t) = o[j];
+    }
+}
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_state_init(vitfp8_scale_state* st, cudaStream_t s) {
+    state_init_kernel<<<1, 1, 0, s>>>(st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_static(vitfp8_scale_state* st, float q, float k, float v, cudaStream_t s) {
+    set_static_kernel<<<1, 1, 0, s>>>(st, q, k, v);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
+                        const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
+                        int D, cudaStream_t s) {
+    dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
+    amax_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant(const vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
+                         const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
+                         int D, int Dp, uint8_t* q8, uint8_t* k8, uint8_t* v8t, int64_t Tv,
+                         cudaStream_t s) {
+    dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
+    int32_t* err = const_cast<int32_t*>(&st->dev_error);
+    quant_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, Dp, q8, k8, v8t, Tv,
+                                             err);
+    return cudaGetLastError();
+}
+
+}  // namespace vitfp8

@@ -1,0 +1,223 @@
+/*
+ * vitfp8 -- FP8 ViT-encoder attention for one GB300 (sm_103a).  C ABI.
+ *
+ * The hot path of one ViT-encoder attention layer, as the pages describe it
+ * ("FP8 ViT Encoder Attention", vLLM docs; "FP8 vision encoder attention",
+ * Sonar):
+ *
+ *   1. per-tensor amax of Q, K and V kept in a 16-entry circular history
+ *      (dynamic scaling) -- or static per-layer scales from a scale file;
+ *   2. on-the-fly FP8 (E4M3) quantization of Q, K and V fused with
+ *      un-padding into a packed variable-length layout;
+ *   3. non-causal variable-length attention over packed multi-image batches
+ *      delimited by cu_seqlens, with FP8 QK^T and FP8 P.V on tensor cores and
+ *      a bf16 output.
+ *
+ * Conventions for every entry point below:
+ *
+ *   - Pointers named d_* and all tensor pointers are DEVICE pointers; h_* are
+ *     HOST pointers.  The caller allocates and frees every buffer (sources,
+ *     codes, outputs, state, workspace).  The library never allocates or
+ *     frees memory on these calls and keeps no mutable global state.
+ *   - All work is enqueued asynchronously on `stream`; nothing synchronises
+ *     with the host except vitfp8_get_device_error /
+ *     vitfp8_get_workspace_error, which synchronise `stream`.
+ *   - Argument errors are detected on the host and returned before any launch
+ *     (VITFP8_ERR_INVALID_ARG / VITFP8_ERR_UNSUPPORTED).  A failed launch
+ *     returns VITFP8_ERR_CUDA.  Errors found on the device (malformed
+ *     cu_seqlens, a bounded wait that timed out) are recorded in a device
+ *     error word and read back with the two *_get_*_error calls.
+ *   - Nothing aborts, traps or throws across this boundary.
+ *   - bf16 tensors are passed as vitfp8_bf16 (the raw 16-bit pattern).
+ *   - Tensors must be 16-byte aligned; sizes and strides are in ELEMENTS.
+ */
+#ifndef VITFP8_H
+#define VITFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t vitfp8_bf16; /* bfloat16 bit pattern */
+
+typedef enum vitfp8_status {
+    VITFP8_OK = 0,
+    VITFP8_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, bad size or stride */
+    VITFP8_ERR_UNSUPPORTED = 2,    /* valid request outside what the kernels cover (e.g. D > 128) */
+    VITFP8_ERR_CUDA = 3,           /* a CUDA runtime / driver call failed */
+    VITFP8_ERR_DEVICE_TIMEOUT = 4, /* device: a bounded wait expired; the kernel returned early */
+    VITFP8_ERR_DEVICE_BOUNDS = 5,  /* device: an index fell outside its buffer and was skipped */
+    VITFP8_ERR_BAD_SEQLENS = 6,    /* device: cu_seqlens not 0 = c0 <= c1 <= ... <= c_B = T */
+    VITFP8_ERR_WORKSPACE = 7       /* workspace missing or smaller than vitfp8_attn_workspace_size */
+} vitfp8_status;
+
+#define VITFP8_RING 16          /* amax history length ("16-entry circular buffer") */
+#define VITFP8_E4M3_MAX 448.0f  /* largest finite E4M3 value */
+#define VITFP8_MAX_HEAD_DIM 128 /* largest head dim the attention kernels take */
+
+/*
+ * One layer's FP8 scale state, DEVICE-resident, one per attention layer.
+ *
+ * Source: "FP8 ViT Encoder Attention", Usage -- a 16-entry circular buffer of
+ * observed Q/K/V amax values drives per-forward scale updates; Calibrate-Once
+ * and Scale File Format -- static per-layer q/k/v values.
+ *
+ * Index t in the [3] arrays is 0 = q, 1 = k, 2 = v.  A "scale value" A is an
+ * amax-like magnitude: dequantisation factor scale = A/448, quantisation
+ * multiplier inv_scale = 448/A (each one IEEE float32 division).  If A == 0
+ * both are 1.  The fields amax_bits and blocks_done are reduction scratch
+ * owned by vitfp8_amax_update; they are zero between calls.
+ */
+typedef struct vitfp8_scale_state {
+    float    hist[3][VITFP8_RING]; /* amax ring per tensor; empty slots hold 0 */
+    int32_t  pos;                  /* slot the next forward writes */
+    int32_t  count;                /* filled slots, <= 16 */
+    int32_t  mode;                 /* 0 dynamic, 1 static */
+    int32_t  dev_error;            /* first device-detected vitfp8_status, 0 if none */
+    float    amax_ref[3];          /* A_t: ring maximum (dynamic) or the static value */
+    float    scale[3];             /* A_t / 448 */
+    float    inv_scale[3];         /* 448 / A_t */
+    float    amax_cur[3];          /* amax of the latest dynamic forward */
+    uint32_t amax_bits[3];         /* scratch: running max of |x| as bf16 magnitude bits */
+    uint32_t blocks_done;          /* scratch: finished blocks of the current amax launch */
+} vitfp8_scale_state;
+
+/*
+ * Where the valid bf16 source rows of Q, K or V live ("un-padding").
+ *
+ * padded = 1: a padded batch -- segment b's token i sits at row b*s_max + i;
+ *             rows i >= L_b are padding and are never read.
+ * padded = 0: packed rows -- segment b's token i sits at row cu_seqlens[b]+i.
+ * Element (row, h, d) is at row*token_stride + h*head_stride + d (elements);
+ * d is contiguous.  token_stride and head_stride must be multiples of 8 so
+ * that every 8-element vector is 16-byte aligned (e.g. a view into a fused
+ * [T, 3, H, D] QKV buffer has token_stride 3*H*D).
+ */
+typedef struct vitfp8_src_layout {
+    int32_t padded;
+    int32_t reserved;
+    int64_t s_max;
+    int64_t token_stride;
+    int64_t head_stride;
+} vitfp8_src_layout;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* vitfp8_status_string(vitfp8_status s);
+
+/* Library ABI version (major*100 + minor). */
+int32_t vitfp8_version(void);
+
+/*
+ * Reset a state to dynamic mode with an empty ring (all slots 0, pos 0,
+ * count 0, scale = inv_scale = 1, dev_error 0, scratch 0).
+ * d_state: device pointer to one vitfp8_scale_state (4-byte aligned).
+ */
+vitfp8_status vitfp8_scale_state_init(vitfp8_scale_state* d_state, cudaStream_t stream);
+
+/*
+ * Switch a state to static mode with the scale-file values q, k, v
+ * ("FP8 ViT Encoder Attention", Scale File Format: e.g. 224, 198, 210).
+ * Each value must be finite and > 0 (else VITFP8_ERR_INVALID_ARG, nothing
+ * launched).  Sets amax_ref = value, scale = value/448, inv_scale = 448/value.
+ */
+vitfp8_status vitfp8_set_static_scales(vitfp8_scale_state* d_state, float q, float k, float v,
+                                       cudaStream_t stream);
+
+/*
+ * Dynamic scaling, one forward ("FP8 ViT Encoder Attention", Usage; Sonar,
+ * Enable FP8 attention): amax of q, k and v over the valid tokens (all heads,
+ * d < D), pushed into the 16-entry ring (push-then-scale), then
+ * amax_ref = max(ring), scale and inv_scale recomputed.  One launch covers
+ * all three tensors; the last block to finish updates the ring.
+ * In static mode the launch returns without touching the state (a no-op).
+ *
+ * q, k, v:        bf16 sources, layout given by *h_layout (host pointer).
+ * d_cu_seqlens:   int32[num_seqs + 1] on the device, 0 = c0 <= ... <= c_B = total_tokens.
+ * total_tokens:   T = c_B (host copy); T == 0 or num_seqs == 0 is a no-op.
+ * H, D:           heads and head dim; D % 8 == 0, 8 <= D <= 256.
+ * Amax follows fmax semantics: NaN ignored, +inf propagates.
+ * Concurrent calls on the same state race (the scratch fields are shared).
+ */
+vitfp8_status vitfp8_amax_update(vitfp8_scale_state* d_state, const vitfp8_bf16* q,
+                                 const vitfp8_bf16* k, const vitfp8_bf16* v,
+                                 const vitfp8_src_layout* h_layout, const int32_t* d_cu_seqlens,
+                                 int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t D,
+                                 cudaStream_t stream);
+
+/*
+ * Quantize + un-pad q, k and v in ONE launch ("FP8 ViT Encoder Attention",
+ * intro and note: Q/K/V quantized on the fly before the attention call,
+ * "quantization kernel launches + un-padding").
+ *
+ * code = E4M3(float32(x) * inv_scale[t]), round to nearest even, saturating
+ * to +-448, NaN -> NaN code; entries d in [D, D_pad) are written as 0x00.
+ *
+ * Outputs (device, caller-allocated):
+ *   q8, k8: uint8 [T][H][D_pad]   packed token order (row t*H + h).
+ *   v8t:    uint8 [H][D_pad][Tv]  V transposed per head, tokens contiguous,
+ *           Tv = vitfp8_vt_stride(T); tokens in [T, Tv) are written as 0x00.
+ * D_pad: multiple of 16, D <= D_pad <= 256.
+ */
+vitfp8_status vitfp8_quantize_unpad(const vitfp8_scale_state* d_state, const vitfp8_bf16* q,
+                                    const vitfp8_bf16* k, const vitfp8_bf16* v,
+                                    const vitfp8_src_layout* h_layout,
+                                    const int32_t* d_cu_seqlens, int32_t num_seqs,
+                                    int32_t total_tokens, int32_t H, int32_t D, int32_t D_pad,
+                                    uint8_t* q8, uint8_t* k8, uint8_t* v8t, cudaStream_t stream);
+
+/* Token stride Tv of the transposed V code buffer: T rounded up to 16. */
+int64_t vitfp8_vt_stride(int32_t total_tokens);
+
+/* Bytes of device workspace vitfp8_attn_varlen(_bf16) needs for num_seqs segments. */
+size_t vitfp8_attn_workspace_size(int32_t num_seqs);
+
+/*
+ * FP8 variable-length non-causal attention ("FP8 ViT Encoder Attention",
+ * intro, Performance; Sonar, Requirements: packed variable-length batches,
+ * per-tensor FP8).
+ *
+ * For each segment b (tokens c_b .. c_{b+1}-1), head h and query i of b:
+ *   s_ij = (q8_i . k8_j) * scale_q * scale_k * sm_scale   over keys j in b only,
+ *   softmax in fp32 (online), P requantized to E4M3 (relative to a
+ *   power-of-two reference) for an FP8 P.V tensor-core product,
+ *   o_i = (sum_j P_ij v8_j) * scale_v / sum_j p_ij, rounded to bf16.
+ * No query attends across a cu_seqlens boundary.
+ *
+ * q8, k8:  uint8 [T][H][D_pad] E4M3 codes; v8t: uint8 [H][D_pad][Tv] (as
+ *          written by vitfp8_quantize_unpad).
+ * d_state: scales read on the device (scale[0..2]).
+ * max_seqlen: host upper bound of the segment lengths (>= every L_b).
+ * D: 8..128, D % 8 == 0; D_pad % 16 == 0, D <= D_pad <= 128.
+ * sm_scale: softmax scale, normally 1/sqrt(D); finite and > 0.
+ * out: bf16 [T][H][D].
+ * d_workspace: >= vitfp8_attn_workspace_size(num_seqs) bytes, 16-byte
+ *          aligned; holds the (longest-first) work list and an error word.
+ *          Calls sharing one workspace must be stream-ordered.
+ */
+vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                                 const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,
+                                 int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens,
+                                 int32_t H, int32_t D, int32_t D_pad, float sm_scale,
+                                 vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
+ * Device error word of a state: *h_out = first vitfp8_status recorded by a
+ * kernel that used d_state (0 if none).  Synchronises `stream`.  h_out: host.
+ */
+vitfp8_status vitfp8_get_device_error(const vitfp8_scale_state* d_state, int32_t* h_out,
+                                      cudaStream_t stream);
+
+/* Same for an attention workspace.  Synchronises `stream`. */
+vitfp8_status vitfp8_get_workspace_error(const void* d_workspace, int32_t* h_out,
+                                         cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VITFP8_H */

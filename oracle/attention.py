@@ -36,9 +36,19 @@ import numpy as np
 from . import e4m3
 
 
+_DECODE = None
+
+
 def dequant(codes, scale):
-    """float64 values of E4M3 codes times the float32 scale."""
-    return e4m3.decode(codes) * np.float64(np.float32(scale))
+    """float64 values of E4M3 codes times the float32 scale.
+
+    Decoding goes through a 256-entry table of ``e4m3.decode`` (the same
+    closed form, evaluated once per code).
+    """
+    global _DECODE
+    if _DECODE is None:
+        _DECODE = e4m3.decode(np.arange(256, dtype=np.uint8))
+    return _DECODE[np.asarray(codes, dtype=np.uint8)] * np.float64(np.float32(scale))
 
 
 def _segments(cu_seqlens):
@@ -60,8 +70,22 @@ def _rows_by_segment(cu_seqlens, rows):
     return out
 
 
+def _attend(q, k, v, sm_scale, p_round):
+    """One (segment, head) block: q [r, D], k [L, D], v [L, Dv] float64 -> [r, Dv]."""
+    sc = (q @ k.T) * float(sm_scale)
+    if p_round:
+        # Power-of-two reference: M = ceil(rowmax / ln 2).
+        M = np.ceil(sc.max(axis=1, keepdims=True) / math.log(2.0))
+        p = np.exp(sc - M * math.log(2.0))
+        pq = e4m3.round_significand(p, 4)
+        return (pq @ v) / p.sum(axis=1, keepdims=True)
+    m = sc.max(axis=1, keepdims=True)
+    p = np.exp(sc - m)
+    return (p @ v) / p.sum(axis=1, keepdims=True)
+
+
 def attention_varlen(qh, kh, vh, cu_seqlens, sm_scale=None, rows=None, p_round=False):
-    """o[T, H, D] float64 (rows not requested stay NaN when ``rows`` is given).
+    """o[T, H, Dv] float64 (rows not requested stay NaN when ``rows`` is given).
 
     qh, kh, vh: float64 [T, H, D] dequantized values (only the true D columns).
     """
@@ -74,20 +98,7 @@ def attention_varlen(qh, kh, vh, cu_seqlens, sm_scale=None, rows=None, p_round=F
     out = np.full((T, H, vh.shape[2]), np.nan, dtype=np.float64)
     for s, e, sel in _rows_by_segment(cu_seqlens, rows):
         for h in range(H):
-            q = qh[sel, h, :]             # [r, D]
-            k = kh[s:e, h, :]             # [L, D]
-            v = vh[s:e, h, :]             # [L, Dv]
-            sc = (q @ k.T) * float(sm_scale)
-            if p_round:
-                # Power-of-two reference: M = ceil(rowmax / ln 2).
-                M = np.ceil(sc.max(axis=1, keepdims=True) / math.log(2.0))
-                p = np.exp(sc - M * math.log(2.0))
-                pq = e4m3.round_significand(p, 4)
-                out[sel, h, :] = (pq @ v) / p.sum(axis=1, keepdims=True)
-            else:
-                m = sc.max(axis=1, keepdims=True)
-                p = np.exp(sc - m)
-                out[sel, h, :] = (p @ v) / p.sum(axis=1, keepdims=True)
+            out[sel, h, :] = _attend(qh[sel, h, :], kh[s:e, h, :], vh[s:e, h, :], sm_scale, p_round)
     return out
 
 
@@ -97,11 +108,28 @@ def attention_varlen_p8(qh, kh, vh, cu_seqlens, sm_scale=None, rows=None):
 
 
 def attention_fp8(q8, k8, v8, scales, cu_seqlens, D, sm_scale=None, rows=None, p_round=False):
-    """Attention on packed [T, H, D_pad] codes with per-tensor scales (q, k, v)."""
-    qh = dequant(q8[:, :, :D], scales[0])
-    kh = dequant(k8[:, :, :D], scales[1])
-    vh = dequant(v8[:, :, :D], scales[2])
-    return attention_varlen(qh, kh, vh, cu_seqlens, sm_scale, rows, p_round)
+    """Attention on packed [T, H, D_pad] E4M3 codes with per-tensor scales (q, k, v).
+
+    Returns [T, H, D], or [len(rows), H, D] in the order of the sorted ``rows``
+    when rows are given.  Dequantizes one (segment, head) slice at a time, so
+    full-size workloads fit in host memory; the arithmetic is that of
+    ``attention_varlen``.
+    """
+    T, H = q8.shape[0], q8.shape[1]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if rows is not None:
+        rows = np.unique(np.asarray(rows, dtype=np.int64))
+    n = T if rows is None else rows.size
+    out = np.full((n, H, D), np.nan, dtype=np.float64)
+    for s, e, sel in _rows_by_segment(cu_seqlens, rows):
+        pos = sel if rows is None else np.searchsorted(rows, sel)
+        for h in range(H):
+            q = dequant(q8[sel, h, :D], scales[0])
+            k = dequant(k8[s:e, h, :D], scales[1])
+            v = dequant(v8[s:e, h, :D], scales[2])
+            out[pos, h, :] = _attend(q, k, v, sm_scale, p_round)
+    return out
 
 
 def attention_bruteforce(qh, kh, vh, cu_seqlens, sm_scale=None):

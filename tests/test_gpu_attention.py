@@ -1,0 +1,179 @@
+"""GPU parity of the FP8 varlen attention kernel against the fp64 oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import scales as oscales
+
+from gpu_util import (assert_attention_ok, compare_attention, cu_tensor, np32, oracle_push, qkv,
+                      sample_rows, vt_to_thd)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vf():
+    import fp8_vision_encoder_gb300 as vf
+    assert torch.cuda.is_available()
+    return vf
+
+
+def _run(vf, seqlens, H, D, seeds, static=None, D_pad=None, outliers=True, per_head_std=False,
+         gen_device="cpu"):
+    cu, cul = cu_tensor(seqlens)
+    st = vf.ScaleState().init()
+    ost = oscales.ScaleState()
+    if static is not None:
+        st.set_static(*static)
+        ost.set_static(*static)
+    for seed in seeds:
+        q, k, v = [t.cuda() for t in workloads.make_qkv(seqlens, H, D, seed, outliers, per_head_std,
+                                                         device=gen_device)]
+        if static is None:
+            vf.amax_update(st, q, k, v, cu)
+            oracle_push(ost, q, k, v)
+    q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu, D_pad=D_pad)
+    ws = vf.Workspace(len(seqlens))
+    out = vf.attn_varlen(q8, k8, v8t, st, cu, max(seqlens) if seqlens else 0, D, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.error() == 0
+    T = sum(seqlens)
+    return dict(out=out, q8=q8, k8=k8, v8=vt_to_thd(v8t, T), v8t=v8t, scales=list(ost.scale),
+                cu=cul, st=st, ws=ws, cu_t=cu, q=q, k=k, v=v)
+
+
+def test_tiny_config(vf):
+    w = workloads.WORKLOADS["tiny"]
+    r = _run(vf, w.seqlens, w.H, w.D, w.seeds)
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], w.D)
+    assert_attention_ok(stats, "tiny")
+
+
+@pytest.mark.parametrize("D", [64, 80, 128])
+def test_ragged_segments(vf, D):
+    seqlens = [1, 127, 128, 129, 300, 17, 0, 5]
+    r = _run(vf, seqlens, 3, D, [21])
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], D)
+    assert_attention_ok(stats, "ragged D=%d" % D)
+
+
+def test_d80_padded_codes(vf):
+    r = _run(vf, [200, 333], 2, 80, [5], D_pad=96, per_head_std=True, outliers=False)
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 80)
+    assert_attention_ok(stats, "d80 D_pad=96")
+
+
+def test_single_long_segment_static(vf):
+    r = _run(vf, [2000], 4, 128, [0], static=(224.0, 198.0, 210.0))
+    rows = sample_rows(r["cu"], 300)
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 128, rows)
+    assert_attention_ok(stats, "2000 static")
+
+
+def test_rescale_path_late_large_score(vf):
+    """A key in a late tile scores far above everything before it: O is rescaled."""
+    seqlens = [1000]
+    H, D = 1, 128
+    cu, cul = cu_tensor(seqlens)
+    g = torch.Generator().manual_seed(3)
+    q = torch.randn(1000, H, D, generator=g) * 0.3
+    k = torch.randn(1000, H, D, generator=g) * 0.3
+    v = torch.randn(1000, H, D, generator=g)
+    k[900] = q.mean(dim=0) * 40.0       # aligned with the average query, large
+    q, k, v = [t.to(torch.bfloat16).cuda() for t in (q, k, v)]
+    st = vf.ScaleState().init()
+    vf.amax_update(st, q, k, v, cu)
+    q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
+    out = vf.attn_varlen(q8, k8, v8t, st, cu, 1000, D)
+    torch.cuda.synchronize()
+    sc = st.read()["scale"]
+    stats = compare_attention(out, q8, k8, vt_to_thd(v8t, 1000), sc, cul, D)
+    assert_attention_ok(stats, "rescale")
+
+
+def test_deterministic_and_no_cross_segment_leakage(vf):
+    seqlens = [300, 129, 500]
+    H, D = 2, 128
+    r = _run(vf, seqlens, H, D, [7])
+    out1 = r["out"].clone()
+    out2 = vf.attn_varlen(r["q8"], r["k8"], r["v8t"], r["st"], r["cu_t"], 500, D)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    # perturb segment 1's keys and values: segments 0 and 2 must not move a bit
+    k8 = r["k8"].clone()
+    v8t = r["v8t"].clone()
+    k8[300:429] = (k8[300:429].to(torch.int32) ^ 0x11).to(torch.uint8) & 0x77
+    v8t[:, :, 300:429] = 0x38
+    out3 = vf.attn_varlen(r["q8"], k8, v8t, r["st"], r["cu_t"], 500, D)
+    torch.cuda.synchronize()
+    a = out1.view(torch.int16)
+    b = out3.view(torch.int16)
+    assert torch.equal(a[:300], b[:300]) and torch.equal(a[429:], b[429:])
+    assert not torch.equal(a[300:429], b[300:429])
+
+
+def test_bad_seqlens_reports_and_writes_nothing(vf):
+    H, D = 2, 128
+    T = 64
+    q8 = torch.zeros((T, H, D), dtype=torch.uint8, device="cuda")
+    v8t = torch.zeros((H, D, vf.vt_stride(T)), dtype=torch.uint8, device="cuda")
+    st = vf.ScaleState().init()
+    out = torch.full((T, H, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    for bad in ([0, 40, 30, 64], [0, 32, 60], [1, 32, 64]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        ws = vf.Workspace(len(bad) - 1)
+        vf.attn_varlen(q8, q8, v8t, st, cu, 64, D, out=out, workspace=ws)
+        assert ws.error() == 6
+    assert torch.all(out.float() == 7.0)
+
+
+def test_empty_inputs_are_noops(vf):
+    st = vf.ScaleState().init()
+    cu = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e = torch.empty((0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    vf.amax_update(st, e, e, e, cu)
+    q8, k8, v8t = vf.quantize_unpad(st, e, e, e, cu)
+    out = vf.attn_varlen(q8, k8, v8t, st, cu, 0, 128)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 2, 128)
+    assert st.read()["count"] == 0
+
+
+@pytest.mark.parametrize("name", ["micro8k", "hd3", "qhd3", "uhd3mix"])
+def test_full_size_sampled_rows(vf, name):
+    """Full-size workloads in the bench's launch configuration, sampled query rows."""
+    w = workloads.WORKLOADS[name]
+    cu, cul = cu_tensor(w.seqlens)
+    st = vf.ScaleState().init()
+    ost = oscales.ScaleState()
+    gen = lambda seed: workloads.make_qkv(w.seqlens, w.H, w.D, seed, w.outliers, w.per_head_std,
+                                          device="cuda")
+    if w.scaling == "static":
+        st.set_static(*w.static)
+        ost.set_static(*w.static)
+        q, k, v = gen(w.seeds[0])
+    elif w.scaling == "calibrated":
+        for seed in w.calib_seeds:
+            q, k, v = gen(seed)
+            vf.amax_update(st, q, k, v, cu)
+            oracle_push(ost, q, k, v)
+        A = [float(np.float32(a) * np.float32(1.5)) for a in st.read()["amax_ref"]]
+        st.set_static(*A)
+        ost.set_static(*A)
+        q, k, v = gen(w.layer_seeds[0])
+    else:
+        seeds = w.seeds[-3:] if name == "hd3" else w.seeds
+        for seed in seeds:
+            q, k, v = gen(seed)
+            vf.amax_update(st, q, k, v, cu)
+            oracle_push(ost, q, k, v)
+    q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
+    out = vf.attn_varlen(q8, k8, v8t, st, cu, w.max_seqlen, w.D)
+    torch.cuda.synchronize()
+    rows = sample_rows(cul, 48, seed=1)
+    stats = compare_attention(out, q8, k8, vt_to_thd(v8t, w.T), list(ost.scale), cul, w.D, rows)
+    assert_attention_ok(stats, name)
