@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libvitfp8.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         "libvitfp8.so is not built (expected at %s); build it with "
-        "`python -m fp8_vision_encoder_gb300.build`" % LIB_PATH)
+        "`python fp8_vision_encoder_gb300/build.py`" % LIB_PATH)
 
 _lib = ctypes.CDLL(LIB_PATH)
 

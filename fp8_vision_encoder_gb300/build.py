@@ -1,6 +1,6 @@
 """Build libvitfp8.so in-tree with nvcc for sm_103a (no cmake, no torch build).
 
-Usage: ``python -m fp8_vision_encoder_gb300.build`` or ``build()``.  The three
+Usage: ``python fp8_vision_encoder_gb300/build.py`` or ``build()``.  The three
 translation units compile in parallel; the CUDA runtime is linked statically
 so the library loads without a separate libcudart on the path.
 """
