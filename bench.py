@@ -1,0 +1,432 @@
+"""Benchmark of the FP8 ViT-encoder attention hot path on GB300.
+
+One step = one encoder forward of the workload: for every layer, quantize +
+un-pad Q/K/V (one launch) and run FP8 variable-length attention (work-list
+launch + attention launch).  Default workload: 3 QHD images packed
+(3 x 14400 tokens), 16 heads, head_dim 128, 24 layers, static scales = 1.5 x
+the amax calibrated over 16 dynamic forwards.  Metric: algorithmic attention
+TFLOP/s (4 * sum L^2 * H * D per layer) including the quantization time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...    # the CPU oracle on a bounded sample
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own copy of
+the workload on its own GPU (independent layers, no collective on the data
+path); the reported value is all ranks' work over the slowest rank's time.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "FP8 varlen ViT-attention TFLOPS incl. quant (3×QHD, d=128); % of FP8 peak"
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor-core ratio
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+class Runner:
+    """Holds a workload's device buffers and runs one step through the C ABI."""
+
+    def __init__(self, vf, w, device, layers=None):
+        self.vf = vf
+        self.w = w
+        self.dev = device
+        self.cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=device)
+        self.D_pad = vf.default_d_pad(w.D)
+        gen = lambda seed: workloads.make_qkv(w.seqlens, w.H, w.D, seed, w.outliers,
+                                              w.per_head_std, device=device)
+        if w.scaling == "calibrated":
+            # Calibrate once: 16 dynamic forwards, then static = 1.5 x ring max.
+            st = vf.ScaleState(device).init()
+            for seed in w.calib_seeds:
+                q, k, v = gen(seed)
+                vf.amax_update(st, q, k, v, self.cu)
+            A = st.read()["amax_ref"]
+            self.static = [float(np.float32(a) * np.float32(1.5)) for a in A]
+            seeds = w.layer_seeds if layers is None else w.layer_seeds[:layers]
+            self.dynamic = False
+        elif w.scaling == "static":
+            self.static = list(w.static)
+            seeds = w.seeds
+            self.dynamic = False
+        else:
+            self.static = None
+            seeds = w.seeds[-1:]
+            self.dynamic = True
+        self.inputs = [gen(s) for s in seeds]
+        self.states = []
+        for _ in self.inputs:
+            st = vf.ScaleState(device)
+            st.init()
+            if self.static is not None:
+                st.set_static(*self.static)
+            self.states.append(st)
+        self.codes = vf.alloc_codes(w.T, w.H, self.D_pad, device)
+        self.out = torch.empty((w.T, w.H, w.D), dtype=torch.bfloat16, device=device)
+        self.ws = vf.Workspace(len(w.seqlens), device)
+        self.layers = len(self.inputs)
+        self.flops_layer = w.flops()
+        self.launches_layer = 3 + (1 if self.dynamic else 0)
+
+    def layer(self, i, stream, ev=None):
+        vf, w = self.vf, self.w
+        q, k, v = self.inputs[i]
+        st = self.states[i]
+        if ev is not None:
+            ev[0].record(stream)
+        if self.dynamic:
+            vf.amax_update(st, q, k, v, self.cu, stream=stream)
+        vf.quantize_unpad(st, q, k, v, self.cu, D_pad=self.D_pad, out=self.codes, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        q8, k8, v8t = self.codes
+        vf.attn_varlen(q8, k8, v8t, st, self.cu, w.max_seqlen, w.D, out=self.out,
+                       workspace=self.ws, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def step(self, stream, evs=None):
+        for i in range(self.layers):
+            self.layer(i, stream, None if evs is None else evs[i])
+
+
+def _quant_bytes(w, dynamic):
+    n = w.T * w.H * w.D
+    return 3 * n * (5 if dynamic else 3)
+
+
+# ----------------------------------------------------------------------------- cpu baseline
+def cpu_oracle_sample(w, seconds_budget=12.0, rows_per_block=None, blocks=None, seed=0):
+    """Time the oracle (as it stands) on whole (segment, head) blocks of one layer.
+
+    Each block: E4M3-quantize that head's q/k/v slices of the segment with the
+    layer's scales, then fp64 attention for its queries over all its keys.
+    Returns (TFLOP/s of algorithmic attention flops, cores, description).
+    """
+    from oracle import attention as oattn
+    from oracle import quant as oquant
+    from oracle import scales as oscales
+
+    q, k, v = workloads.make_qkv(w.seqlens, w.H, w.D, seed, w.outliers, w.per_head_std, device="cpu")
+    st = oscales.ScaleState()
+    st.push([oscales.amax(t.float().numpy()) for t in (q, k, v)])
+    order = [(b, h) for b in range(len(w.seqlens)) for h in range(w.H)]
+    cu = w.cu_seqlens
+    flops = 0.0
+    done = 0
+    t0 = time.perf_counter()
+    for b, h in order:
+        s, e = cu[b], cu[b + 1]
+        L = e - s
+        R = L if rows_per_block is None else min(L, rows_per_block)
+        qs = q[s:s + R, h:h + 1].float().numpy()
+        ks = k[s:e, h:h + 1].float().numpy()
+        vs = v[s:e, h:h + 1].float().numpy()
+        c = [oquant.quantize(x, st.inv_scale[t]) for t, x in enumerate((qs, ks, vs))]
+        _attend_block(oattn, c, st.scale, R, L, w.D)
+        flops += 4.0 * R * L * w.D
+        done += 1
+        if (blocks is not None and done >= blocks) or (blocks is None and
+                                                        time.perf_counter() - t0 > seconds_budget):
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    rows_desc = "all queries" if rows_per_block is None else "%d queries" % rows_per_block
+    desc = ("%d of %d (segment, head) blocks of one %s layer: E4M3 quantize of the block's "
+            "q/k/v slices + fp64 attention (%s x all keys of the segment)"
+            % (done, len(order), w.name, rows_desc))
+    return flops / dt / 1e12, cores, desc, dt
+
+
+def _attend_block(oattn, c, scales, R, L, D):
+    """fp64 attention of R queries against L keys of one (segment, head) block."""
+    q = oattn.dequant(c[0][:, 0, :D], scales[0])
+    k = oattn.dequant(c[1][:, 0, :D], scales[1])
+    v = oattn.dequant(c[2][:, 0, :D], scales[2])
+    return oattn._attend(q, k, v, 1.0 / math.sqrt(D), False)
+
+
+# ----------------------------------------------------------------------------- main
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    w = workloads.WORKLOADS[args.workload]
+    vals = []
+    desc = ""
+    cores = 0
+    total = 0.0
+    for i in range(args.warmup + args.steps):
+        v, cores, desc, dt = cpu_oracle_sample(w, rows_per_block=1024, blocks=1, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+            total += dt
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qhd3", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=None, help="limit layers (qhd3 only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    args = ap.parse_args()
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import fp8_vision_encoder_gb300 as vf
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    w = workloads.WORKLOADS[args.workload]
+    run = Runner(vf, w, dev, layers=args.layers)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(3, args.warmup)):
+        run.step(stream)
+    torch.cuda.synchronize(dev)
+
+    # per-kernel events in a separate (untimed-for-value) pass of the same steps
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(run.layers)]
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for s in range(args.steps):
+        run.step(stream, evs[s])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if pg:
+        pg.barrier()
+    ms = start.elapsed_time(stop)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    quant_ms = [e[0].elapsed_time(e[1]) for st in evs for e in st]
+    attn_ms = [e[1].elapsed_time(e[2]) for st in evs for e in st]
+    assert run.ws.error() == 0, "attention workspace reported a device error"
+
+    flops_step = run.flops_layer * run.layers
+    value = ws * flops_step * args.steps / (ms * 1e-3) / 1e12
+    peaks, peak_kind = _peaks()
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    attn_avg = statistics.mean(attn_ms)
+    quant_avg = statistics.mean(quant_ms)
+    achieved = run.flops_layer / (attn_avg * 1e-3) / 1e12
+    qbytes = _quant_bytes(w, run.dynamic)
+    quant_gbs = qbytes / (quant_avg * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
+        "config": {"workload": w.desc, "name": w.name, "tokens": w.T, "segments": w.seqlens[:8],
+                   "heads": w.H, "head_dim": w.D, "layers": run.layers,
+                   "static_scales": run.static,
+                   "l2": "inputs larger than L2 (each layer reads its own %.0f MB of bf16 q/k/v)"
+                         % (3 * w.T * w.H * w.D * 2 / 1e6),
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "frac_of_fp8_peak": value / fp8_peak,
+        "roofline": {"bound": "tensor", "kernel": "attn_fp8 (work-list + attention launch)",
+                     "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp8_peak, "traffic": None,
+                     "peak_source": "%s bf16 sustained x %.0f (fp8/bf16 nominal ratio)"
+                                    % (peak_kind, FP8_PER_BF16)},
+        "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": quant_gbs / peaks["hbm_gbs"],
+                           "algorithmic_bytes": qbytes, "peak_source": peak_kind},
+        "breakdown_us": {"quant": 1e3 * quant_avg, "attn": 1e3 * attn_avg},
+        "gpu_launches": run.launches_layer * run.layers * args.steps,
+        "clocks": clocks,
+    }
+
+    # end to end through the public API with host buffers
+    if not args.no_e2e:
+        line["e2e"] = e2e(vf, run, stream, dev, args.e2e_steps, ws, pg)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, cores, desc, dt = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def e2e(vf, run, stream, dev, steps, ws, pg):
+    """Same metric with pinned host inputs copied in and the output copied out every layer."""
+    w = run.w
+    host_in = []
+    for trio in run.inputs:
+        hs = []
+        for t in trio:
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            hs.append(h)
+        host_in.append(hs)
+    host_out = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+    dev_in = [torch.empty_like(t) for t in run.inputs[0]]
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0]) * run.layers
+    d2h = host_out.numel() * host_out.element_size() * run.layers
+
+    def one_step():
+        for i in range(run.layers):
+            for d, h in zip(dev_in, host_in[i]):
+                d.copy_(h, non_blocking=True)
+            st = run.states[i]
+            if run.dynamic:
+                vf.amax_update(st, *dev_in, run.cu, stream=stream)
+            vf.quantize_unpad(st, *dev_in, run.cu, D_pad=run.D_pad, out=run.codes, stream=stream)
+            q8, k8, v8t = run.codes
+            vf.attn_varlen(q8, k8, v8t, st, run.cu, w.max_seqlen, w.D, out=run.out,
+                           workspace=run.ws, stream=stream)
+            host_out.copy_(run.out, non_blocking=True)
+
+    one_step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    val = ws * run.flops_layer * run.layers * steps / (ms * 1e-3) / 1e12
+    return {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -18,11 +18,14 @@
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.
 //
 // Softmax in log2 units: x = S_raw * c, c = scale_q scale_k sm_scale log2(e).
-// Each row keeps an integer reference m_ref; P' = E4M3(2^(x - m_ref + 4)).
-// O and l are rescaled (by an exact power of two) only when a tile's max
-// exceeds m_ref + 4, which keeps P' <= 256 < 448 (no saturation) and makes the
-// E4M3 rounding of P independent of the reference chosen.  l sums the
-// unrounded fp32 values.  o = O * scale_v / l, rounded to bf16.
+// Each row keeps an integer reference m_ref = ceil(running max of x) and
+// requantizes P' = E4M3(2^(x - m_ref + 8)), so the row maximum lands in
+// (128, 256] (below 448: no saturation) and small weights keep E4M3's full
+// range.  When a tile raises ceil(max), O and l are rescaled by the exact
+// power of two 2^(m_old - m_new); because every reference is a power of two,
+// the rounded significands equal those taken against the final reference.
+// l sums the rounded P' values themselves (the weights applied to V sum to
+// one).  o = O * scale_v / l, rounded to bf16.
 //
 // Keys are walked in tiles starting at floor16(segment start) so that every
 // V^T tile starts at a 16-byte-aligned token coordinate; keys outside the
@@ -50,8 +53,7 @@ constexpr int NUM_THREADS = 320;
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int TILE = 128 * 128;          // bytes of one 128-row x 128-byte tile
-constexpr int HEADROOM = 4;              // rescale when max grows past m_ref + HEADROOM
-constexpr float PSHIFT = 8 - HEADROOM;   // P' = 2^(x - m_ref + PSHIFT) <= 2^8
+constexpr float PSHIFT = 8.0f;           // P' = 2^(x - m_ref + 8) <= 2^8
 
 constexpr int SM_Q = 0;
 constexpr int SM_K = SM_Q + NQT * TILE;
@@ -341,7 +343,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             bool need = false;
             if (j == 0) {
                 m_ref = ceilf(xmax);
-            } else if (xmax > m_ref + float(HEADROOM)) {
+            } else if (xmax > m_ref) {
                 const float mnew = ceilf(xmax);
                 oscale = exp2_int(m_ref - mnew);
                 l *= oscale;
@@ -350,18 +352,28 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             const float bias = PSHIFT - m_ref;
             uint32_t pk[32];
-            float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float p0 = ex2_approx(fmaf(sf[4 * i + 0], c, bias));
                 const float p1 = ex2_approx(fmaf(sf[4 * i + 1], c, bias));
                 const float p2 = ex2_approx(fmaf(sf[4 * i + 2], c, bias));
                 const float p3 = ex2_approx(fmaf(sf[4 * i + 3], c, bias));
-                ls0 += p0 + p1;
-                ls1 += p2 + p3;
                 pk[i] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
             }
-            l += ls0 + ls1;
+            // Row sum of the rounded P values that enter the P.V product, so the
+            // weights applied to V sum to one: E4M3 -> f16 is exact, 16 values
+            // are summed in f16x2, each partial sum is added in fp32.
+            float ls = 0.f;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                uint32_t a = hadd2(e4m3x2_to_f16x2(pk[4 * g] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g] >> 16));
+                uint32_t b = hadd2(e4m3x2_to_f16x2(pk[4 * g + 1] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g + 1] >> 16));
+                uint32_t d = hadd2(e4m3x2_to_f16x2(pk[4 * g + 2] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g + 2] >> 16));
+                uint32_t e = hadd2(e4m3x2_to_f16x2(pk[4 * g + 3] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g + 3] >> 16));
+                const float2 f = f16x2_to_float2(hadd2(hadd2(a, b), hadd2(d, e)));
+                ls += f.x + f.y;
+            }
+            l += ls;
 
             if (j > 0) {
                 ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_PVDONE + w), (j - 1) & 1, abort_flag, err));

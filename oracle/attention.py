@@ -21,12 +21,16 @@ Readings taken where the pages are silent:
 
 ``attention_varlen`` is that plain definition.  ``attention_varlen_p8`` adds
 the one rounding step the FP8 hot path takes inside the softmax -- P is
-requantized to E4M3 before the P.V product -- under this reading: P is
-rounded to E4M3 significand precision (4 significant bits, nearest-even)
-relative to a power-of-two reference 2^M_i, M_i = ceil(max_j s_ij / ln 2),
-while the row sum l_i uses the unrounded p.  Because the reference is a power
-of two, the rounded significands do not depend on which power of two the
-online softmax uses, so the variant is fixed by the data alone.
+requantized to E4M3 before the P.V product -- under this reading:
+
+  p_ij  = exp(s_ij - M_i ln 2),  M_i = ceil(max_j s_ij / ln 2)  (p_ij <= 1),
+  P'_ij = E4M3(2^8 p_ij)         (row maximum lands in (128, 256], below 448),
+  o_i   = sum_j P'_ij v_hat_j / sum_j P'_ij,
+
+i.e. the row sum adds the same rounded values, so the weights applied to V sum
+to one.  The reference is a power of two, so within E4M3's normal range the
+rounded significands do not depend on which power of two an online softmax
+happens to use.
 """
 
 import math
@@ -35,6 +39,7 @@ import numpy as np
 
 from . import e4m3
 
+P_SHIFT = 8  # P' = E4M3(2^8 p), p <= 1
 
 _DECODE = None
 
@@ -74,11 +79,11 @@ def _attend(q, k, v, sm_scale, p_round):
     """One (segment, head) block: q [r, D], k [L, D], v [L, Dv] float64 -> [r, Dv]."""
     sc = (q @ k.T) * float(sm_scale)
     if p_round:
-        # Power-of-two reference: M = ceil(rowmax / ln 2).
+        # Power-of-two reference 2^M, M = ceil(rowmax / ln 2); P' = E4M3(2^8 p).
         M = np.ceil(sc.max(axis=1, keepdims=True) / math.log(2.0))
         p = np.exp(sc - M * math.log(2.0))
-        pq = e4m3.round_significand(p, 4)
-        return (pq @ v) / p.sum(axis=1, keepdims=True)
+        pq = e4m3.decode(e4m3.encode(np.ldexp(p, P_SHIFT)))
+        return (pq @ v) / pq.sum(axis=1, keepdims=True)
     m = sc.max(axis=1, keepdims=True)
     p = np.exp(sc - m)
     return (p @ v) / p.sum(axis=1, keepdims=True)

@@ -166,12 +166,51 @@ def test_p8_error_within_e4m3_bound_and_nonzero():
     cu = [0, 64]
     a = attention.attention_varlen(q, k, v, cu)
     b = attention.attention_varlen_p8(q, k, v, cu)
-    # bound: each P entry moves by at most 2^-4 of itself -> |b - a| <= 2^-4 * sum p|v| / l
-    # which is <= 2^-4 * max|v| per row and head.
-    bound = 2.0 ** -4 * np.abs(v).max(axis=0, keepdims=True) + 1e-12
+    # Each weight p_j/l moves by at most a factor (1 +- 2^-4)/(1 -+ 2^-4) and both
+    # weight sets sum to one, so |b - a| <= (2^-3 / (1 - 2^-4)) * (max v - min v) / 2.
+    rng_v = v.max(axis=0, keepdims=True) - v.min(axis=0, keepdims=True)
+    bound = (2.0 ** -3 / (1 - 2.0 ** -4)) * rng_v / 2 + 1e-12
     assert np.all(np.abs(b - a) <= bound)
     rel = np.sqrt(np.mean((b - a) ** 2)) / np.sqrt(np.mean(a ** 2))
     assert 1e-3 < rel < 6e-2
+
+
+def test_p8_weights_sum_to_one():
+    # Constant V comes back exactly and one-hot V rows sum to one: the rounded
+    # weights are normalised by their own sum.
+    L, D = 40, 8
+    q, k, _ = _rand_qkv(L, 1, D, seed=11)
+    v = np.full((L, 1, 4), -1.75)
+    o = attention.attention_varlen_p8(q, k, v, [0, L])
+    assert np.allclose(o, -1.75, rtol=0, atol=1e-14)
+    v1 = np.zeros((L, 1, L))
+    v1[np.arange(L), 0, np.arange(L)] = 1.0
+    o1 = attention.attention_varlen_p8(q, k, v1, [0, L])
+    assert np.allclose(o1.sum(axis=2), 1.0, atol=1e-14)
+    # and every weight is an E4M3-representable value over the common sum
+    w = o1[:, 0, :] * (1.0 / o1[:, 0, :].max(axis=1, keepdims=True))
+    assert np.all(w >= 0)
+
+
+def test_p8_underflow_drops_far_keys():
+    # Keys 20 binades below the maximum give 2^8 p = 2^-12 < 2^-10 (half the
+    # smallest E4M3 subnormal): they round to zero and o is the top key's value.
+    L = 6
+    q = np.zeros((L, 1, 1))
+    k = np.zeros((L, 1, 1))
+    q[:, 0, 0] = 1.0
+    k[:, 0, 0] = -20 * np.log(2.0)
+    k[2, 0, 0] = 0.0
+    v = np.arange(L, dtype=np.float64).reshape(L, 1, 1) + 0.5
+    o = attention.attention_varlen_p8(q, k, v, [0, L], sm_scale=1.0)
+    assert np.all(o == 2.5)
+    # 17 binades below: 2^-9 is the smallest subnormal and survives
+    k[:, 0, 0] = -17 * np.log(2.0)
+    k[2, 0, 0] = 0.0
+    o = attention.attention_varlen_p8(q, k, v, [0, L], sm_scale=1.0)
+    w_far = 2.0 ** -9
+    expect = (2.5 * 256 + w_far * (v[:, 0, 0].sum() - 2.5)) / (256 + 5 * w_far)
+    assert np.allclose(o, expect, rtol=1e-12)
 
 
 def test_p8_does_not_depend_on_reference_power_of_two():
