@@ -48,6 +48,24 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def _profile_traffic(md_name, sources):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", md_name)).read()
+        m = hashlib.sha256()
+        for src in sources:
+            with open(os.path.join(ROOT, "fp8_vision_encoder_gb300", "csrc", src), "rb") as f:
+                m.update(f.read())
+        sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text).group(1)
+        if sha != m.hexdigest()[:len(sha)]:
+            return None
+        return int(re.search(r"dram_bytes_per_launch:\s*(\d+)", text).group(1))
+    except (OSError, AttributeError, ValueError):
+        return None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -353,12 +371,17 @@ def main():
         "frac_of_fp8_peak": value / fp8_peak,
         "roofline": {"bound": "tensor", "kernel": "attn_fp8 (work-list + attention launch)",
                      "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": None,
+                     "frac": achieved / fp8_peak,
+                     "traffic": (_profile_traffic("attn_fp8_qhd3.md", ["attn_fp8.cu", "ptx.cuh"])
+                                 if w.name == "qhd3" else None),
+                     "algorithmic_bytes": 3 * w.T * w.H * w.D + 2 * w.T * w.H * w.D,
                      "peak_source": "%s bf16 sustained x %.0f (fp8/bf16 nominal ratio)"
                                     % (peak_kind, FP8_PER_BF16)},
         "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": quant_gbs / peaks["hbm_gbs"],
-                           "algorithmic_bytes": qbytes, "peak_source": peak_kind},
+                           "algorithmic_bytes": qbytes, "peak_source": peak_kind,
+                           "traffic": (_profile_traffic("quant_qhd3.md", ["quant.cu", "ptx.cuh"])
+                                       if w.name == "qhd3" and not run.dynamic else None)},
         "breakdown_us": {"quant": 1e3 * quant_avg, "attn": 1e3 * attn_avg},
         "gpu_launches": run.launches_layer * run.layers * args.steps,
         "clocks": clocks,
