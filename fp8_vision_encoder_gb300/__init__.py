@@ -105,6 +105,9 @@ _ws_size = _sig("vitfp8_attn_workspace_size", ctypes.c_size_t, [_i32])
 _attn = _sig("vitfp8_attn_varlen", ctypes.c_int,
              [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
               ctypes.c_size_t, _vp])
+_attn_noalloc = _sig("vitfp8_attn_varlen_noalloc", ctypes.c_int,
+                     [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp])
+NOALLOC_MAX_SEQS = 4096
 _get_err = _sig("vitfp8_get_device_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 _get_ws_err = _sig("vitfp8_get_workspace_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 
@@ -254,4 +257,24 @@ def attn_varlen(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, ou
     _check(_attn(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq, int(max_seqlen),
                  int(T), int(H), int(D), int(D_pad), float(sm_scale), _ptr(out),
                  _ptr(workspace.buf), workspace.nbytes, _stream(stream)), "vitfp8_attn_varlen")
+    return out
+
+
+def attn_varlen_noalloc(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, out=None,
+                        stream=None):
+    """FP8 varlen attention through the entry point that allocates nothing.
+
+    For callers that cannot allocate device memory: the work list lives in a
+    fixed device array inside the library (at most NOALLOC_MAX_SEQS segments).
+    ``out`` should be passed pre-allocated by such callers.
+    """
+    nseq = _cu_info(cu_seqlens)
+    T, H, D_pad = q8.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q8.device)
+    _check(_attn_noalloc(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq,
+                         int(max_seqlen), int(T), int(H), int(D), int(D_pad), float(sm_scale),
+                         _ptr(out), _stream(stream)), "vitfp8_attn_varlen_noalloc")
     return out

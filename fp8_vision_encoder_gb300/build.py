@@ -1,6 +1,6 @@
 """Build libvitfp8.so in-tree with nvcc for sm_103a (no cmake, no torch build).
 
-Usage: ``python fp8_vision_encoder_gb300/build.py`` or ``build()``.  The three
+Usage: ``python fp8_vision_encoder_gb300/build.py`` or ``build()``.  The
 translation units compile in parallel; the CUDA runtime is linked statically
 so the library loads without a separate libcudart on the path.
 """
@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvitfp8.so")
-SOURCES = ["api.cu", "quant.cu", "attn_fp8.cu"]
+SOURCES = ["api.cu", "quant.cu", "attn_fp8.cu", "attn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

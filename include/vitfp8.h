@@ -205,6 +205,40 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
                                  vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
 
+/* Largest num_seqs vitfp8_attn_varlen_noalloc accepts. */
+#define VITFP8_NOALLOC_MAX_SEQS 4096
+
+/*
+ * vitfp8_attn_varlen without a workspace argument: it allocates nothing and
+ * needs nothing allocated by the caller beyond the inputs and the output.
+ * The pages have no counterpart; this entry point exists for callers that
+ * cannot allocate device memory -- e.g. a plugin handed only raw input/output
+ * pointers and no allocator, a serving host whose device memory pool is fixed
+ * at start-up, or a latency-critical loop that cannot afford the device
+ * synchronisation that cudaMalloc may cause.
+ *
+ * Arguments, layouts and the computation are exactly those of
+ * vitfp8_attn_varlen.  The work list lives instead in a fixed device array
+ * inside the library (about 33 KB; every GPU that loads the library keeps it
+ * until the process exits), sized for at most VITFP8_NOALLOC_MAX_SEQS
+ * segments: num_seqs above that returns VITFP8_ERR_UNSUPPORTED without
+ * launching.  The first call on each device looks up that array's device
+ * address (cudaGetSymbolAddress) with the device current; make that first
+ * call before any stream capture.  Every call on a device shares the one
+ * array and rewrites all of it that it reads, so nothing carries over between
+ * calls; calls that overlap on the GPU (different streams, or different
+ * host threads, without ordering) race on it.  Device-detected errors
+ * (malformed cu_seqlens, a timed-out wait) leave the output unwritten and are
+ * not reported by this entry point; use vitfp8_attn_varlen with a workspace
+ * to read them.
+ */
+vitfp8_status vitfp8_attn_varlen_noalloc(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                                         const vitfp8_scale_state* d_state,
+                                         const int32_t* d_cu_seqlens, int32_t num_seqs,
+                                         int32_t max_seqlen, int32_t total_tokens, int32_t H,
+                                         int32_t D, int32_t D_pad, float sm_scale, vitfp8_bf16* out,
+                                         cudaStream_t stream);
+
 /*
  * Device error word of a state: *h_out = first vitfp8_status recorded by a
  * kernel that used d_state (0 if none).  Synchronises `stream`.  h_out: host.
