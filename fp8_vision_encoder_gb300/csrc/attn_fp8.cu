@@ -9,13 +9,23 @@
 // segment and head) against every key tile of that segment:
 //
 //   warp 8      TMA producer: Q tiles once, then K and V^T tiles through a
-//               3-stage shared-memory ring (128-byte swizzle).
-//   warp 9      MMA issuer (one thread): S_w = Q_w K^T and O_w += P_w V into
-//               tensor memory, tcgen05.mma kind::f8f6f4 (E4M3 x E4M3 -> F32).
+//               shared-memory ring (128-byte swizzle).
+//   warp 9      MMA issuer (one thread), tcgen05.mma kind::f8f6f4 (E4M3 x E4M3
+//               -> F32) into tensor memory.  Per key tile j and query tile w:
+//               O_w += P_w(j) V_j with P_w read from TMEM, then immediately
+//               S_w(j+1) = Q_w K_{j+1}^T into the same TMEM columns.
 //   warps 0-3   softmax for query tile 0, warps 4-7 for query tile 1: one
-//               thread per query row, reading its S row from TMEM.
+//               thread per query row; S row from TMEM into registers, P row
+//               (E4M3) back into the first 32 columns of that S region.
 //
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.
+// TMEM (512 columns): S_0/P_0 | S_1/P_1 | O_0 | O_1, 128 columns each.  P lives
+// in TMEM so the P.V product reads only V from shared memory: with both
+// operands in shared memory an FP8 128x128x32 MMA needs the whole shared-memory
+// bandwidth.  MMAs issued by one thread execute in order, so (a) S_w(j+1) is
+// written only after P_w(j) has been consumed and (b) when S_w(j) is complete,
+// every earlier P.V into O_w is complete too: the softmax may rescale O_w as
+// soon as it sees S_w(j).  The two query tiles alternate on the tensor core
+// (one computes its softmax while the other's P.V and S run).
 //
 // Softmax in log2 units: x = S_raw * c, c = scale_q scale_k sm_scale log2(e).
 // Each row keeps an integer reference m_ref = ceil(running max of x) and
@@ -49,7 +59,7 @@ constexpr int NQT = 2;                   // query tiles per CTA
 constexpr int ROWS_PER_ITEM = BM * NQT;  // queries per work item
 constexpr int BN = 128;                  // keys per tile
 constexpr int NST = 3;                   // K/V pipeline stages
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 320;         // 8 softmax warps, TMA warp, MMA warp
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int TILE = 128 * 128;          // bytes of one 128-row x 128-byte tile
@@ -58,18 +68,16 @@ constexpr float PSHIFT = 8.0f;           // P' = 2^(x - m_ref + 8) <= 2^8
 constexpr int SM_Q = 0;
 constexpr int SM_K = SM_Q + NQT * TILE;
 constexpr int SM_V = SM_K + NST * TILE;
-constexpr int SM_P = SM_V + NST * TILE;
-constexpr int SM_BAR = SM_P + NQT * TILE;
+constexpr int SM_BAR = SM_V + NST * TILE;
 // barrier indices
 constexpr int B_QFULL = 0;
 constexpr int B_KFULL = 1;
 constexpr int B_VFULL = B_KFULL + NST;
 constexpr int B_KVEMPTY = B_VFULL + NST;
-constexpr int B_SFULL = B_KVEMPTY + NST;   // [NQT]
-constexpr int B_SFREE = B_SFULL + NQT;     // [NQT]
-constexpr int B_PFULL = B_SFREE + NQT;     // [NQT]
-constexpr int B_PVDONE = B_PFULL + NQT;    // [NQT]
-constexpr int B_FINAL = B_PVDONE + NQT;
+constexpr int B_SFULL = B_KVEMPTY + NST;   // [NQT]: S_w(j) (and every earlier P.V) complete
+constexpr int B_PFULL = B_SFULL + NQT;     // [NQT]: P_w(j) written to TMEM by the 4 warps
+constexpr int B_OREADY = B_PFULL + NQT;    // [NQT]: last P.V into O_w complete
+constexpr int B_FINAL = B_OREADY + NQT;
 constexpr int NBAR = B_FINAL + 1;
 constexpr int SM_TMEMPTR = SM_BAR + NBAR * 8;
 constexpr int SM_ABORT = SM_TMEMPTR + 4;
@@ -172,9 +180,8 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         for (int w = 0; w < NQT; ++w) {
             mbar_init(BAR(B_SFULL + w), 1);
-            mbar_init(BAR(B_SFREE + w), 4);
             mbar_init(BAR(B_PFULL + w), 4);
-            mbar_init(BAR(B_PVDONE + w), 1);
+            mbar_init(BAR(B_OREADY + w), 1);
         }
         mbar_init(BAR(B_FINAL), 1);
         *abort_flag = 0;
@@ -227,27 +234,26 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0) {
             const uint32_t idS = make_idesc(0, BM, BN);
             const uint32_t idPV = make_idesc(0, BM, p.DV);
+            // Descriptors are built once: within a 128-byte swizzled row a
+            // 32-byte K step adds 2 to the encoded start address, a stage adds
+            // TILE / 16.  Issuing then costs a few integer adds per MMA.
+            const uint64_t dQ[NQT] = {sw128_kmajor_desc(sb + SM_Q), sw128_kmajor_desc(sb + SM_Q + TILE)};
+            const uint64_t dK0 = sw128_kmajor_desc(sb + SM_K);
+            const uint64_t dV0 = sw128_kmajor_desc(sb + SM_V);
+            const int KS = p.KS;
             auto issue_S = [&](int w, int s) {
-                tc_fence_after();
-                for (int kk = 0; kk < p.KS; ++kk)
-                    umma_f8(tmem + uint32_t(w * BN),
-                            sw128_kmajor_desc(sb + SM_Q + w * TILE + kk * 32),
-                            sw128_kmajor_desc(sb + SM_K + s * TILE + kk * 32), idS, kk > 0);
+                const uint64_t dq = dQ[w];
+                const uint64_t dk = dK0 + uint64_t(s * (TILE >> 4));
+                const uint32_t dS = tmem + uint32_t(w * BN);
+                umma_f8(dS, dq, dk, idS, 0u);
+                for (int kk = 1; kk < KS; ++kk)
+                    umma_f8(dS, dq + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
                 tc_commit(BAR(B_SFULL + w));
-            };
-            auto issue_PV = [&](int w, int s, bool acc) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BN / 32; ++kk)
-                    umma_f8(tmem + uint32_t(2 * BN + w * BN),
-                            sw128_kmajor_desc(sb + SM_P + w * TILE + kk * 32),
-                            sw128_kmajor_desc(sb + SM_V + s * TILE + kk * 32), idPV,
-                            (acc || kk > 0) ? 1u : 0u);
-                tc_commit(BAR(B_PVDONE + w));
             };
             bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
                       bwait(BAR(B_KFULL + 0), 0, abort_flag, err);
             if (ok) {
+                tc_fence_after();
                 issue_S(0, 0);
                 issue_S(1, 0);
             }
@@ -257,24 +263,25 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const bool nxt = j + 1 < nkv;
                 const int s1 = (j + 1) % NST;
                 const uint32_t ph1 = ((j + 1) / NST) & 1;
-                if (nxt) {
-                    ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err) &&
-                         bwait(BAR(B_SFREE + 0), j & 1, abort_flag, err);
-                    if (!ok) break;
-                    issue_S(0, s1);
+                if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
+                if (nxt && !(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
+                const uint64_t dv = dV0 + uint64_t(s * (TILE >> 4));
+                for (int w = 0; w < NQT; ++w) {
+                    // P_w(j) in TMEM -> O_w += P_w(j) V_j, then S_w(j+1) over P_w.
+                    if (!(ok = bwait(BAR(B_PFULL + w), j & 1, abort_flag, err))) break;
+                    tc_fence_after();
+                    const uint32_t dO = tmem + uint32_t(2 * BN + w * BN);
+                    const uint32_t aP = tmem + uint32_t(w * BN);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 32; ++kk)
+                        umma_f8_ts(dO, aP + uint32_t(8 * kk), dv + uint64_t(2 * kk), idPV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                    if (nxt)
+                        issue_S(w, s1);
+                    else
+                        tc_commit(BAR(B_OREADY + w));
                 }
-                ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err) &&
-                     bwait(BAR(B_PFULL + 0), j & 1, abort_flag, err);
                 if (!ok) break;
-                issue_PV(0, s, j > 0);
-                if (nxt) {
-                    ok = bwait(BAR(B_SFREE + 1), j & 1, abort_flag, err);
-                    if (!ok) break;
-                    issue_S(1, s1);
-                }
-                ok = bwait(BAR(B_PFULL + 1), j & 1, abort_flag, err);
-                if (!ok) break;
-                issue_PV(1, s, j > 0);
                 tc_commit(BAR(B_KVEMPTY + s));
             }
             // Every MMA issued above has completed before TMEM is released.
@@ -282,7 +289,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int spin = 0; spin < (1 << 24); ++spin)
                 if (mbar_try_wait(BAR(B_FINAL), 0)) break;
         }
-    } else {
+    } else if (warp < 8) {
         // ------------------------------------------------ softmax (warps 0..7)
         const int w = warp >> 2;              // query tile
         const int sub = warp & 3;             // TMEM lane quarter
@@ -293,11 +300,11 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t tS = tmem + lane_off + uint32_t(w * BN);
         const uint32_t tO = tmem + lane_off + uint32_t(2 * BN + w * BN);
         const float c = p.st->scale[0] * p.st->scale[1] * p.sm_scale * 1.4426950408889634f;
-        uint8_t* prow = smem + SM_P + w * TILE + (r >> 3) * 1024 + (r & 7) * 128;
         float m_ref = 0.0f;
         float l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
+            // S_w(j) complete; so is every P.V of earlier tiles into O_w.
             ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + w), j & 1, abort_flag, err));
             if (!ok) break;
             tc_fence_after();
@@ -310,9 +317,6 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             reg_fence32(s1);
             reg_fence32(s2);
             reg_fence32(s3);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_SFREE + w));
 
             float sf[128];
 #pragma unroll
@@ -332,11 +336,11 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
 #pragma unroll
-            for (int i = 4; i < 128; i += 4) {
-                mx0 = fmaxf(mx0, sf[i]);
-                mx1 = fmaxf(mx1, sf[i + 1]);
-                mx2 = fmaxf(mx2, sf[i + 2]);
-                mx3 = fmaxf(mx3, sf[i + 3]);
+            for (int i = 4; i < 128; i += 8) {
+                mx0 = fmax3(mx0, sf[i], sf[i + 1]);
+                mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
+                mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
+                mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
             }
             const float xmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
             float oscale = 1.0f;
@@ -351,58 +355,59 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 need = true;
             }
             const float bias = PSHIFT - m_ref;
+
+            // P' = E4M3(2^(x - m_ref + 8)), four keys per 32-bit word, and the
+            // row sum of those same rounded values (E4M3 -> f16 exact, f16x2
+            // adds over 16 keys, fp32 across), so the weights applied to V sum
+            // to one.
             uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float p0 = ex2_approx(fmaf(sf[4 * i + 0], c, bias));
-                const float p1 = ex2_approx(fmaf(sf[4 * i + 1], c, bias));
-                const float p2 = ex2_approx(fmaf(sf[4 * i + 2], c, bias));
-                const float p3 = ex2_approx(fmaf(sf[4 * i + 3], c, bias));
-                pk[i] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
-            }
-            // Row sum of the rounded P values that enter the P.V product, so the
-            // weights applied to V sum to one: E4M3 -> f16 is exact, 16 values
-            // are summed in f16x2, each partial sum is added in fp32.
             float ls = 0.f;
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                uint32_t a = hadd2(e4m3x2_to_f16x2(pk[4 * g] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g] >> 16));
-                uint32_t b = hadd2(e4m3x2_to_f16x2(pk[4 * g + 1] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g + 1] >> 16));
-                uint32_t d = hadd2(e4m3x2_to_f16x2(pk[4 * g + 2] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g + 2] >> 16));
-                uint32_t e = hadd2(e4m3x2_to_f16x2(pk[4 * g + 3] & 0xFFFFu), e4m3x2_to_f16x2(pk[4 * g + 3] >> 16));
+            for (int ch = 0; ch < 8; ++ch) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int i = ch * 16 + q * 4;
+                    pk[ch * 4 + q] = cvt_e4m3x4(ex2_approx(fmaf(sf[i + 0], c, bias)),
+                                                ex2_approx(fmaf(sf[i + 1], c, bias)),
+                                                ex2_approx(fmaf(sf[i + 2], c, bias)),
+                                                ex2_approx(fmaf(sf[i + 3], c, bias)));
+                }
+                const uint32_t* wd = pk + ch * 4;
+                const uint32_t a = hadd2(e4m3x2_to_f16x2(wd[0] & 0xFFFFu), e4m3x2_to_f16x2(wd[0] >> 16));
+                const uint32_t b = hadd2(e4m3x2_to_f16x2(wd[1] & 0xFFFFu), e4m3x2_to_f16x2(wd[1] >> 16));
+                const uint32_t d = hadd2(e4m3x2_to_f16x2(wd[2] & 0xFFFFu), e4m3x2_to_f16x2(wd[2] >> 16));
+                const uint32_t e = hadd2(e4m3x2_to_f16x2(wd[3] & 0xFFFFu), e4m3x2_to_f16x2(wd[3] >> 16));
                 const float2 f = f16x2_to_float2(hadd2(hadd2(a, b), hadd2(d, e)));
                 ls += f.x + f.y;
             }
             l += ls;
 
-            if (j > 0) {
-                ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_PVDONE + w), (j - 1) & 1, abort_flag, err));
-                if (!ok) break;
-            }
             if (__any_sync(0xFFFFFFFFu, need)) {
-                tc_fence_after();
+                // O_w holds every P.V before tile j (complete, see above).
+                const uint64_t s2v = f32x2_pack(oscale, oscale);
                 for (int cc = 0; cc < p.DV; cc += 16) {
                     uint32_t o[16];
                     tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
                     tmem_ld_wait16(o);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * oscale);
+                    for (int q = 0; q < 16; q += 2) {
+                        float a0, a1;
+                        f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(o[q]), __uint_as_float(o[q + 1])), s2v),
+                                     a0, a1);
+                        o[q] = __float_as_uint(a0);
+                        o[q + 1] = __float_as_uint(a1);
+                    }
                     tmem_st_32x32b_x16(tO + uint32_t(cc), o);
                 }
-                tmem_st_wait();
             }
-            // P row -> shared memory, K-major with 128-byte swizzle.
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            }
-            fence_proxy_async_smem();
+            // P row into the first 32 columns of this row's S region.
+            tmem_st_32x32b_x32(tS, pk);
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_PFULL + w));
         }
-        if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_PVDONE + w), (nkv - 1) & 1, abort_flag, err));
+        if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OREADY + w), 0, abort_flag, err));
         if (ok) {
             tc_fence_after();
             const float oscale = p.st->scale[2] / l;
