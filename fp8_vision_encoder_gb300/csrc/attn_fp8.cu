@@ -245,9 +245,13 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const uint64_t dq = dQ[w];
                 const uint64_t dk = dK0 + uint64_t(s * (TILE >> 4));
                 const uint32_t dS = tmem + uint32_t(w * BN);
-                umma_f8(dS, dq, dk, idS, 0u);
-                for (int kk = 1; kk < KS; ++kk)
-                    umma_f8(dS, dq + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
+                if (KS == 4) {
+                    umma_f8_ss_k4(dS, dq, dk, idS, 0u);
+                } else {
+                    umma_f8(dS, dq, dk, idS, 0u);
+                    for (int kk = 1; kk < KS; ++kk)
+                        umma_f8(dS, dq + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
+                }
                 tc_commit(BAR(B_SFULL + w));
             };
             bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
@@ -272,10 +276,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tc_fence_after();
                     const uint32_t dO = tmem + uint32_t(2 * BN + w * BN);
                     const uint32_t aP = tmem + uint32_t(w * BN);
-#pragma unroll
-                    for (int kk = 0; kk < BN / 32; ++kk)
-                        umma_f8_ts(dO, aP + uint32_t(8 * kk), dv + uint64_t(2 * kk), idPV,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_f8_ts_k4(dO, aP, dv, idPV, j > 0 ? 1u : 0u);   // K = 128 keys
                     if (nxt)
                         issue_S(w, s1);
                     else
