@@ -107,6 +107,9 @@ _attn = _sig("vitfp8_attn_varlen", ctypes.c_int,
               ctypes.c_size_t, _vp])
 _attn_noalloc = _sig("vitfp8_attn_varlen_noalloc", ctypes.c_int,
                      [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp])
+_attn_bf16 = _sig("vitfp8_attn_varlen_bf16", ctypes.c_int,
+                  [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, ctypes.c_size_t,
+                   _vp])
 NOALLOC_MAX_SEQS = 4096
 _get_err = _sig("vitfp8_get_device_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 _get_ws_err = _sig("vitfp8_get_workspace_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
@@ -257,6 +260,26 @@ def attn_varlen(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, ou
     _check(_attn(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq, int(max_seqlen),
                  int(T), int(H), int(D), int(D_pad), float(sm_scale), _ptr(out),
                  _ptr(workspace.buf), workspace.nbytes, _stream(stream)), "vitfp8_attn_varlen")
+    return out
+
+
+def attn_varlen_bf16(q, k, v, cu_seqlens, max_seqlen, sm_scale=None, out=None, workspace=None,
+                     stream=None):
+    """BF16 varlen attention on bf16 [T, H, D] q, k, v -> bf16 [T, H, D]."""
+    nseq = _cu_info(cu_seqlens)
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError("q, k, v must be contiguous bf16 tensors of one shape [T, H, D]")
+    T, H, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        workspace = Workspace(nseq, q.device)
+    _check(_attn_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseq, int(max_seqlen), int(T),
+                      int(H), int(D), float(sm_scale), _ptr(out), _ptr(workspace.buf),
+                      workspace.nbytes, _stream(stream)), "vitfp8_attn_varlen_bf16")
     return out
 
 

@@ -146,6 +146,29 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
                            reinterpret_cast<uint16_t*>(out), d_workspace, stream);
 }
 
+vitfp8_status vitfp8_attn_varlen_bf16(const vitfp8_bf16* q, const vitfp8_bf16* k,
+                                      const vitfp8_bf16* v, const int32_t* d_cu_seqlens,
+                                      int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens,
+                                      int32_t H, int32_t D, float sm_scale, vitfp8_bf16* out,
+                                      void* d_workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
+    if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || H <= 0) return VITFP8_ERR_INVALID_ARG;
+    if (D < 8 || (D & 7)) return VITFP8_ERR_INVALID_ARG;
+    if (D > VITFP8_MAX_HEAD_DIM) return VITFP8_ERR_UNSUPPORTED;
+    if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f)) return VITFP8_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_tokens == 0) return VITFP8_OK;
+    if (!q || !k || !v || !d_cu_seqlens || !out) return VITFP8_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        !aligned4(d_cu_seqlens))
+        return VITFP8_ERR_INVALID_ARG;
+    if (!d_workspace || !aligned16(d_workspace) || workspace_bytes < ws_bytes(num_seqs))
+        return VITFP8_ERR_WORKSPACE;
+    return launch_attn_bf16(reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k),
+                            reinterpret_cast<const uint16_t*>(v), d_cu_seqlens, num_seqs,
+                            total_tokens, H, D, sm_scale, reinterpret_cast<uint16_t*>(out),
+                            d_workspace, stream);
+}
+
 vitfp8_status vitfp8_get_device_error(const vitfp8_scale_state* d_state, int32_t* h_out,
                                       cudaStream_t stream) {
     if (!d_state || !h_out) return VITFP8_ERR_INVALID_ARG;

@@ -48,6 +48,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "attn_common.cuh"
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -84,55 +85,7 @@ constexpr int SM_ABORT = SM_TMEMPTR + 4;
 constexpr int SM_USED = SM_ABORT + 4;
 constexpr int SMEM_BYTES = SM_USED + 1024;  // + slack to align the base to 1024
 constexpr uint32_t TMEM_COLS = 512;
-constexpr long long WAIT_LIMIT = 1000000000LL;  // cycles (~0.5 s) before a wait gives up
 }  // namespace fa
-
-struct AttnParams {
-    const int32_t* cu;
-    const int32_t* order;
-    const int32_t* prefix;
-    WsHeader* ws;
-    const vitfp8_scale_state* st;
-    uint16_t* out;
-    int nseq, T, H, D, DV, KS;
-    float sm_scale;
-};
-
-// Bounded wait: true when the phase with `parity` completed; false if the CTA
-// aborted or this wait timed out (which sets the abort flag and the error).
-__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      int32_t* err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > fa::WAIT_LIMIT) {
-                *abort_flag = 1;
-                record_error(err, VITFP8_ERR_DEVICE_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                   "+r"(r[30]), "+r"(r[31]));
-}
-
-// 2^k for an integer-valued float k in [-126, 0].
-__device__ __forceinline__ float exp2_int(float k) {
-    int e = int(k) + 127;
-    e = e < 1 ? 1 : e;
-    return __int_as_float(e << 23);
-}
 
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,

@@ -158,6 +158,25 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab, int M, int N) {
     return (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// Same, with B transposed (MN-major B operand, bit 16).
+__host__ __device__ constexpr uint32_t make_idesc_bmn(uint32_t ab, int M, int N) {
+    return make_idesc(ab, M, N) | (1u << 16);
+}
+
+// Shared-memory matrix descriptor, MN-major, 128-byte swizzle: the MN
+// dimension is contiguous in 128-byte rows (64 bf16), one row per K index;
+// 8 K-rows form a 1024-byte atom.  LBO = byte distance between 64-element MN
+// groups, SBO = byte distance between 8-row K groups.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
+    return d;
+}
+
 // Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B,
 // 8-row atoms of 1024 B stacked at SBO = 1024 B.  `saddr` is the shared
 // address of the first row (atom base 1024-aligned, plus a K offset of a
@@ -316,6 +335,23 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
         : "=f"(lo), "=f"(hi)
         : "r"(v));
     return make_float2(lo, hi);
+}
+// Two float32 -> bf16x2, round to nearest even; `lo` in bits 0..15.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// D[tmem] (+)= A[tmem] * B[smem], BF16 x BF16 -> F32 (A row i in lane i, two
+// bf16 K elements per 32-bit column).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

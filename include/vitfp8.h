@@ -205,6 +205,34 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
                                  vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
 
+/*
+ * BF16 variable-length non-causal attention, the comparison path of
+ * "FP8 ViT Encoder Attention", Performance (the BF16 column of the kernel
+ * and encoder tables): the same segment-masked attention as
+ * vitfp8_attn_varlen, computed from the bf16 inputs directly, with no scales
+ * and no quantization step.
+ *
+ * For each segment b, head h and query i of b:
+ *   s_ij = (q_i . k_j) * sm_scale over keys j in b only (BF16 x BF16 -> fp32
+ *   on the tensor cores), online softmax in fp32, P rounded to bf16 for the
+ *   P.V product, o_i = (sum_j P_ij v_j) / sum_j P_ij (fp32 sum of the
+ *   rounded weights, as in vitfp8_attn_varlen), rounded to bf16.
+ *
+ * q, k, v: bf16 [T][H][D], packed token order, rows contiguous (device).
+ * D: 8..128, D % 8 == 0.  max_seqlen, sm_scale, out and d_workspace as for
+ * vitfp8_attn_varlen (the same workspace size).
+ * Errors: VITFP8_ERR_INVALID_ARG for bad sizes, null or misaligned (16-byte)
+ * pointers; VITFP8_ERR_UNSUPPORTED for D > 128; VITFP8_ERR_WORKSPACE for a
+ * missing or short workspace; malformed cu_seqlens and timed-out waits are
+ * recorded in the workspace error word (vitfp8_get_workspace_error).
+ */
+vitfp8_status vitfp8_attn_varlen_bf16(const vitfp8_bf16* q, const vitfp8_bf16* k,
+                                      const vitfp8_bf16* v, const int32_t* d_cu_seqlens,
+                                      int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens,
+                                      int32_t H, int32_t D, float sm_scale, vitfp8_bf16* out,
+                                      void* d_workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
+
 /* Largest num_seqs vitfp8_attn_varlen_noalloc accepts. */
 #define VITFP8_NOALLOC_MAX_SEQS 4096
 
