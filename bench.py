@@ -296,6 +296,7 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="limit layers (qhd3 only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison column")
     ap.add_argument("--e2e-steps", type=int, default=2)
     args = ap.parse_args()
     ws, rank, local = _dist()
@@ -372,7 +373,8 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "attn_fp8 (work-list + attention launch)",
                      "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp8_peak,
-                     "traffic": (_profile_traffic("attn_fp8_qhd3.md", ["attn_fp8.cu", "ptx.cuh"])
+                     "traffic": (_profile_traffic("attn_fp8_qhd3.md",
+                                                  ["attn_fp8.cu", "attn_common.cuh", "ptx.cuh"])
                                  if w.name == "qhd3" else None),
                      "algorithmic_bytes": 3 * w.T * w.H * w.D + 2 * w.T * w.H * w.D,
                      "peak_source": "%s bf16 sustained x %.0f (fp8/bf16 nominal ratio)"
@@ -387,6 +389,11 @@ def main():
         "clocks": clocks,
     }
 
+    # the BF16 path built the same way, on the same layers (timed separately)
+    if not args.no_bf16:
+        line["bf16_path"] = bf16_column(vf, run, stream, dev, args.steps, peaks, peak_kind,
+                                        1e3 * attn_avg, 1e3 * (attn_avg + quant_avg))
+
     # end to end through the public API with host buffers
     if not args.no_e2e:
         line["e2e"] = e2e(vf, run, stream, dev, args.e2e_steps, ws, pg)
@@ -399,6 +406,50 @@ def main():
     if pg:
         pg.destroy_process_group()
     return 0
+
+
+def bf16_column(vf, run, stream, dev, steps, peaks, peak_kind, fp8_attn_us, fp8_layer_us):
+    """BF16 attention (vitfp8_attn_varlen_bf16) on each layer's bf16 q, k, v.
+
+    Same layers, same output buffer and workspace as the FP8 step; no scales
+    and no quantization.  Timed with CUDA events on the launching stream.
+    """
+    w = run.w
+
+    def one_step(evs=None):
+        for i, (q, k, v) in enumerate(run.inputs):
+            if evs is not None:
+                evs[i][0].record(stream)
+            vf.attn_varlen_bf16(q, k, v, run.cu, w.max_seqlen, out=run.out, workspace=run.ws,
+                                stream=stream)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(3):
+        one_step()
+    torch.cuda.synchronize(dev)
+    n = max(1, min(steps, 3))
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(run.layers)]
+           for _ in range(n)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s_ in range(n):
+        one_step(evs[s_])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    assert run.ws.error() == 0, "attention workspace reported a device error (bf16)"
+    ms = start.elapsed_time(stop) / n
+    attn_us = 1e3 * statistics.mean(e[0].elapsed_time(e[1]) for st in evs for e in st)
+    bf16_peak = peaks["bf16_tflops_sustained"]
+    achieved = run.flops_layer / (attn_us * 1e-6) / 1e12
+    return {"value": run.flops_layer * run.layers / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": ms, "attn_us": attn_us, "dtype": "bf16",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+                         "peak_source": "%s bf16 sustained" % peak_kind},
+            "fp8_attn_speedup": attn_us / fp8_attn_us,
+            "fp8_with_quant_speedup": attn_us / fp8_layer_us}
 
 
 def e2e(vf, run, stream, dev, steps, ws, pg):

@@ -29,8 +29,8 @@ __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile in
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((it & 7u) == 0) {
             if (*abort_flag) return false;
             if (clock64() - t0 > ATTN_WAIT_LIMIT) {
                 *abort_flag = 1;
@@ -49,6 +49,13 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
                    "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
                    "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
                    "+r"(r[30]), "+r"(r[31]));
+}
+
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
 // 2^k for an integer-valued float k in [-126, 0].

@@ -5,45 +5,52 @@
 // seq_len 8192.  "FP8 vision encoder attention" (Sonar), Requirements: packed
 // variable-length image batches with per-tensor FP8 scales.
 //
-// One CTA computes 2 query tiles of 128 rows (256 consecutive queries of one
-// segment and head) against every key tile of that segment:
+// One CTA computes one query tile of 128 rows (128 consecutive queries of one
+// segment and head) against every key tile of 256 keys of that segment:
 //
-//   warp 8      TMA producer: Q tiles once, then K and V^T tiles through a
-//               shared-memory ring (128-byte swizzle).
+//   warp 8      TMA producer: the Q tile once, then K tiles (256 keys x 128 d)
+//               and V^T tiles (d x 256 keys) through a shared-memory ring
+//               (128-byte swizzle).
 //   warp 9      MMA issuer (one thread), tcgen05.mma kind::f8f6f4 (E4M3 x E4M3
-//               -> F32) into tensor memory.  Per key tile j and query tile w:
-//               O_w += P_w(j) V_j with P_w read from TMEM, then immediately
-//               S_w(j+1) = Q_w K_{j+1}^T into the same TMEM columns.
-//   warps 0-3   softmax for query tile 0, warps 4-7 for query tile 1: one
-//               thread per query row; S row from TMEM into registers, P row
-//               (E4M3) back into the first 32 columns of that S region.
+//               -> F32) into tensor memory: S(j+1) = Q K_{j+1}^T (N = 256) as
+//               soon as the softmax has read S(j), and O += P(j) V_j (P read
+//               from TMEM) as soon as P(j) is written.
+//   warps 0-7   softmax, two threads per query row: warp w and warp w + 4 read
+//               the same TMEM lanes (rows 32(w%4) ..), warps 0-3 the keys
+//               0..127 of a tile and warps 4-7 the keys 128..255.  The two
+//               halves of a row swap their partial maxima through shared memory.
 //
-// TMEM (512 columns): S_0/P_0 | S_1/P_1 | O_0 | O_1, 128 columns each.  P lives
-// in TMEM so the P.V product reads only V from shared memory: with both
-// operands in shared memory an FP8 128x128x32 MMA needs the whole shared-memory
-// bandwidth.  MMAs issued by one thread execute in order, so (a) S_w(j+1) is
-// written only after P_w(j) has been consumed and (b) when S_w(j) is complete,
-// every earlier P.V into O_w is complete too: the softmax may rescale O_w as
-// soon as it sees S_w(j).  The two query tiles alternate on the tensor core
-// (one computes its softmax while the other's P.V and S run).
+// TMEM (512 columns): S in 0..255 (fp32, 256 keys), O in 256..399, P in
+// 448..511 (E4M3, four keys per column).  Because P has its own columns, the
+// next S can be computed while the softmax works on the current one: in steady
+// state the softmax never waits for the tensor core.  A single thread needs
+// about as long to issue one MMA as the tensor core needs to run a 128x128x32
+// one; the N = 256 S products halve the number of S instructions.
 //
 // Softmax in log2 units: x = S_raw * c, c = scale_q scale_k sm_scale log2(e).
 // Each row keeps an integer reference m_ref = ceil(running max of x) and
 // requantizes P' = E4M3(2^(x - m_ref + 8)), so the row maximum lands in
-// (128, 256] (below 448: no saturation) and small weights keep E4M3's full
-// range.  When a tile raises ceil(max), O and l are rescaled by the exact
-// power of two 2^(m_old - m_new); because every reference is a power of two,
-// the rounded significands equal those taken against the final reference.
+// (128, 448) (no saturation) and small weights keep E4M3's full range.  The
+// reference moves only when a tile's maximum exceeds m_ref by more than 0.8
+// (P' would pass 2^8.8): then m_ref = ceil(max) and O and l are rescaled by
+// the exact power of two 2^(m_old - m_new).  Because every reference is a
+// power of two, the rounded significands equal those taken against the final
+// reference (only weights in E4M3's subnormal range, below 2^-6 / 2^8.8 of
+// the row maximum, can round differently).
 // l sums the rounded P' values themselves (the weights applied to V sum to
-// one).  o = O * scale_v / l, rounded to bf16.
+// one): each V^T tile carries 16 extra rows of E4M3 ones below its d rows, so
+// the P.V product also accumulates l = sum_k P'_k into O's column d = DV, in
+// fp32 on the tensor core and rescaled with O.  o = O * scale_v / l, rounded to
+// bf16.
 //
 // Keys are walked in tiles starting at floor16(segment start) so that every
 // V^T tile starts at a 16-byte-aligned token coordinate; keys outside the
 // segment are masked to -inf (only the first and last tile need it).
 //
-// Every wait on an mbarrier is bounded; on expiry the CTA records
-// VITFP8_ERR_DEVICE_TIMEOUT in the workspace error word, all roles leave their
-// loops, wait (bounded) for their own async work, free TMEM and return.
+// Every wait (mbarrier or shared-memory handshake) is bounded; on expiry the
+// CTA records VITFP8_ERR_DEVICE_TIMEOUT in the workspace error word, all roles
+// leave their loops, wait (bounded) for their own async work, free TMEM and
+// return.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -55,37 +62,74 @@
 namespace vitfp8 {
 
 namespace fa {
-constexpr int BM = 128;                  // query rows per tile
-constexpr int NQT = 2;                   // query tiles per CTA
-constexpr int ROWS_PER_ITEM = BM * NQT;  // queries per work item
-constexpr int BN = 128;                  // keys per tile
+constexpr int BM = 128;                  // query rows per CTA
+constexpr int ROWS_PER_ITEM = BM;        // queries per work item
+constexpr int BN = 256;                  // keys per tile
+constexpr int HALF = BN / 2;             // keys per softmax thread and tile
 constexpr int NST = 3;                   // K/V pipeline stages
 constexpr int NUM_THREADS = 320;         // 8 softmax warps, TMA warp, MMA warp
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
-constexpr int TILE = 128 * 128;          // bytes of one 128-row x 128-byte tile
-constexpr float PSHIFT = 8.0f;           // P' = 2^(x - m_ref + 8) <= 2^8
+constexpr int QBYTES = BM * 128;         // Q tile: 128 rows x 128 bytes
+constexpr int KBYTES = BN * 128;         // K tile: 256 rows x 128 bytes
+constexpr int VBLK = 144 * 128;          // V^T block: up to 128 d-rows + 16 rows of ones, x 128 keys
+constexpr int VBYTES = 2 * VBLK;         // V^T tile: two key blocks
+constexpr float PSHIFT = 8.0f;           // P' = 2^(x - m_ref + 8)
+constexpr float SLACK = 0.8f;            // x may exceed m_ref by this: P' <= 2^8.8 < 448
 
 constexpr int SM_Q = 0;
-constexpr int SM_K = SM_Q + NQT * TILE;
-constexpr int SM_V = SM_K + NST * TILE;
-constexpr int SM_BAR = SM_V + NST * TILE;
+constexpr int SM_K = SM_Q + QBYTES;
+constexpr int SM_V = SM_K + NST * KBYTES;
+constexpr int SM_XM = SM_V + NST * VBYTES;       // [2 parities][2 halves][128 rows] x 8 B
+constexpr int SM_BAR = SM_XM + 2 * 2 * BM * 8;
 // barrier indices
 constexpr int B_QFULL = 0;
 constexpr int B_KFULL = 1;
 constexpr int B_VFULL = B_KFULL + NST;
 constexpr int B_KVEMPTY = B_VFULL + NST;
-constexpr int B_SFULL = B_KVEMPTY + NST;   // [NQT]: S_w(j) (and every earlier P.V) complete
-constexpr int B_PFULL = B_SFULL + NQT;     // [NQT]: P_w(j) written to TMEM by the 4 warps
-constexpr int B_OREADY = B_PFULL + NQT;    // [NQT]: last P.V into O_w complete
-constexpr int B_FINAL = B_OREADY + NQT;
+constexpr int B_SFULL = B_KVEMPTY + NST;   // S(j) complete in TMEM
+constexpr int B_SFREE = B_SFULL + 1;       // S(j) read by all 8 softmax warps
+constexpr int B_PFULL = B_SFREE + 1;       // P(j) written by all 8 softmax warps
+constexpr int B_OFULL = B_PFULL + 1;       // P(j) V_j (and every earlier MMA) complete
+constexpr int B_FINAL = B_OFULL + 1;
 constexpr int NBAR = B_FINAL + 1;
 constexpr int SM_TMEMPTR = SM_BAR + NBAR * 8;
 constexpr int SM_ABORT = SM_TMEMPTR + 4;
 constexpr int SM_USED = SM_ABORT + 4;
 constexpr int SMEM_BYTES = SM_USED + 1024;  // + slack to align the base to 1024
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 448;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 }  // namespace fa
+
+// Swap one 32-bit value with the partner thread (same row, other key half)
+// through shared memory: the value and a tag are written as one 8-byte word;
+// the partner's word is polled until it carries the same tag.  Bounded like
+// every other wait; false when the CTA aborts or the wait times out.
+__device__ __forceinline__ bool pair_swap(uint32_t mine_addr, uint32_t other_addr, uint32_t value,
+                                          uint32_t tag, uint32_t& other, volatile int* abort_flag,
+                                          int32_t* err) {
+    asm volatile("st.volatile.shared.v2.b32 [%0], {%1, %2};" ::"r"(mine_addr), "r"(value), "r"(tag)
+                 : "memory");
+    const long long t0 = clock64();
+    for (uint32_t it = 0;; ++it) {
+        uint32_t v, t;
+        asm volatile("ld.volatile.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v), "=r"(t) : "r"(other_addr)
+                     : "memory");
+        if (t == tag) {
+            other = v;
+            return true;
+        }
+        if ((it & 15u) == 15u) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > ATTN_WAIT_LIMIT) {
+                *abort_flag = 1;
+                record_error(err, VITFP8_ERR_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
 
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -95,7 +139,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int total = p.ws->total_items;
     if (item >= total) return;
 
-    // ---- work item -> (segment, head, query tile pair)
+    // ---- work item -> (segment, head, query tile)
     int lo = 0, hi = p.nseq - 1;  // largest pos with prefix[pos] <= item
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -124,6 +168,18 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // Exchange words start with a tag no handshake uses.
+    for (int i = threadIdx.x; i < (SM_BAR - SM_XM) / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(smem + SM_XM)[i] = 0xFFFFFFFFu;
+    // Rows DV..DV+15 of every V^T block hold E4M3 1.0 (0x38) for good: the
+    // TMA boxes cover rows 0..DV-1 only.  (Uniform bytes: the swizzle does not
+    // matter.)  The tensor core reads them through the async proxy.
+    for (int i = threadIdx.x; i < NST * 2 * 16 * 32; i += blockDim.x) {
+        const int blk = i / (16 * 32);
+        const int w = i - blk * (16 * 32);
+        reinterpret_cast<uint32_t*>(smem + SM_V + blk * VBLK + p.DV * 128)[w] = 0x38383838u;
+    }
+    fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_QFULL), 1);
         for (int s = 0; s < NST; ++s) {
@@ -131,11 +187,10 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(BAR(B_VFULL + s), 1);
             mbar_init(BAR(B_KVEMPTY + s), 1);
         }
-        for (int w = 0; w < NQT; ++w) {
-            mbar_init(BAR(B_SFULL + w), 1);
-            mbar_init(BAR(B_PFULL + w), 4);
-            mbar_init(BAR(B_OREADY + w), 1);
-        }
+        mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_SFREE), 8);
+        mbar_init(BAR(B_PFULL), 8);
+        mbar_init(BAR(B_OFULL), 1);
         mbar_init(BAR(B_FINAL), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -155,19 +210,19 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(BAR(B_QFULL), NQT * TILE);
-            for (int w = 0; w < NQT; ++w)
-                tma_load_3d(sb + SM_Q + w * TILE, &tmQ, BAR(B_QFULL), 0, h, q0 + w * BM);
-            const uint32_t vbytes = uint32_t(p.DV) * 128u;
+            mbar_arrive_expect_tx(BAR(B_QFULL), QBYTES);
+            tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, h, q0);
+            const uint32_t vbytes = 2u * uint32_t(p.DV) * 128u;
             int j = 0;
             for (; j < nkv; ++j) {
                 const int s = j % NST;
                 if (j >= NST && !bwait(BAR(B_KVEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
                 const int key0 = kbase + j * BN;
-                mbar_arrive_expect_tx(BAR(B_KFULL + s), TILE);
-                tma_load_3d(sb + SM_K + s * TILE, &tmK, BAR(B_KFULL + s), 0, h, key0);
+                mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
+                tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, key0);
                 mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
-                tma_load_3d(sb + SM_V + s * TILE, &tmV, BAR(B_VFULL + s), key0, 0, h);
+                tma_load_3d(sb + SM_V + s * VBYTES, &tmV, BAR(B_VFULL + s), key0, 0, h);
+                tma_load_3d(sb + SM_V + s * VBYTES + VBLK, &tmV, BAR(B_VFULL + s), key0 + HALF, 0, h);
             }
             if (*abort_flag) {
                 // Let the copies this thread started land before the CTA exits.
@@ -185,81 +240,90 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idS = make_idesc(0, BM, BN);
-            const uint32_t idPV = make_idesc(0, BM, p.DV);
+            const uint32_t idS = make_idesc(0, BM, BN);      // 128 x 256 per S product
+            const uint32_t idPV = make_idesc(0, BM, p.DV + 16);   // d columns + the l column block
             // Descriptors are built once: within a 128-byte swizzled row a
-            // 32-byte K step adds 2 to the encoded start address, a stage adds
-            // TILE / 16.  Issuing then costs a few integer adds per MMA.
-            const uint64_t dQ[NQT] = {sw128_kmajor_desc(sb + SM_Q), sw128_kmajor_desc(sb + SM_Q + TILE)};
+            // 32-byte K step adds 2 to the encoded start address; a stage or a
+            // block adds its byte offset / 16.
+            const uint64_t dQ = sw128_kmajor_desc(sb + SM_Q);
             const uint64_t dK0 = sw128_kmajor_desc(sb + SM_K);
             const uint64_t dV0 = sw128_kmajor_desc(sb + SM_V);
+            const uint32_t tS = tmem + TM_S, tO = tmem + TM_O, tP = tmem + TM_P;
             const int KS = p.KS;
-            auto issue_S = [&](int w, int s) {
-                const uint64_t dq = dQ[w];
-                const uint64_t dk = dK0 + uint64_t(s * (TILE >> 4));
-                const uint32_t dS = tmem + uint32_t(w * BN);
+            auto issue_S = [&](int s) {
+                const uint64_t dk = dK0 + uint64_t(s * (KBYTES >> 4));
                 if (KS == 4) {
-                    umma_f8_ss_k4(dS, dq, dk, idS, 0u);
+                    umma_f8_ss_k4(tS, dQ, dk, idS, 0u);
                 } else {
-                    umma_f8(dS, dq, dk, idS, 0u);
+                    umma_f8(tS, dQ, dk, idS, 0u);
                     for (int kk = 1; kk < KS; ++kk)
-                        umma_f8(dS, dq + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
+                        umma_f8(tS, dQ + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
                 }
-                tc_commit(BAR(B_SFULL + w));
+                tc_commit(BAR(B_SFULL));
             };
             bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
                       bwait(BAR(B_KFULL + 0), 0, abort_flag, err);
             if (ok) {
                 tc_fence_after();
-                issue_S(0, 0);
-                issue_S(1, 0);
+                issue_S(0);
             }
+            int s = 0, s1 = 1 % NST;
+            uint32_t ph = 0, ph1 = NST == 1 ? 1u : 0u;
             for (int j = 0; ok && j < nkv; ++j) {
-                const int s = j % NST;
-                const uint32_t ph = (j / NST) & 1;
-                const bool nxt = j + 1 < nkv;
-                const int s1 = (j + 1) % NST;
-                const uint32_t ph1 = ((j + 1) / NST) & 1;
-                if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
-                if (nxt && !(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
-                const uint64_t dv = dV0 + uint64_t(s * (TILE >> 4));
-                for (int w = 0; w < NQT; ++w) {
-                    // P_w(j) in TMEM -> O_w += P_w(j) V_j, then S_w(j+1) over P_w.
-                    if (!(ok = bwait(BAR(B_PFULL + w), j & 1, abort_flag, err))) break;
+                if (j + 1 < nkv) {
+                    // S(j+1) as soon as K_{j+1} is in and every softmax warp has read S(j).
+                    if (!(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
+                    if (!(ok = bwait(BAR(B_SFREE), j & 1, abort_flag, err))) break;
                     tc_fence_after();
-                    const uint32_t dO = tmem + uint32_t(2 * BN + w * BN);
-                    const uint32_t aP = tmem + uint32_t(w * BN);
-                    umma_f8_ts_k4(dO, aP, dv, idPV, j > 0 ? 1u : 0u);   // K = 128 keys
-                    if (nxt)
-                        issue_S(w, s1);
-                    else
-                        tc_commit(BAR(B_OREADY + w));
+                    issue_S(s1);
                 }
-                if (!ok) break;
+                // O += P(j) V_j: 256 keys in 8 steps of 32, keys 0..127 from
+                // V^T block 0 and P columns 0..31, keys 128..255 from block 1
+                // and P columns 32..63.
+                if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
+                if (!(ok = bwait(BAR(B_PFULL), j & 1, abort_flag, err))) break;
+                tc_fence_after();
+                const uint64_t dv = dV0 + uint64_t(s * (VBYTES >> 4));
+                umma_f8_ts_k4(tO, tP, dv, idPV, j > 0 ? 1u : 0u);
+                umma_f8_ts_k4(tO, tP + 32u, dv + uint64_t(VBLK >> 4), idPV, 1u);
+                tc_commit(BAR(B_OFULL));
                 tc_commit(BAR(B_KVEMPTY + s));
+                s = s1;
+                ph = ph1;
+                if (++s1 == NST) {
+                    s1 = 0;
+                    ph1 ^= 1u;
+                }
             }
             // Every MMA issued above has completed before TMEM is released.
             tc_commit(BAR(B_FINAL));
             for (int spin = 0; spin < (1 << 24); ++spin)
                 if (mbar_try_wait(BAR(B_FINAL), 0)) break;
         }
-    } else if (warp < 8) {
+    } else {
         // ------------------------------------------------ softmax (warps 0..7)
-        const int w = warp >> 2;              // query tile
+        const int half = warp >> 2;           // keys half*128 .. half*128+127 of each tile
         const int sub = warp & 3;             // TMEM lane quarter
         const int r = sub * 32 + lane;        // row inside the query tile
-        const int qrow = q0 + w * BM + r;     // packed token index of this row
+        const int qrow = q0 + r;              // packed token index of this row
         const bool row_valid = qrow < seg_e;
         const uint32_t lane_off = uint32_t(sub * 32) << 16;
-        const uint32_t tS = tmem + lane_off + uint32_t(w * BN);
-        const uint32_t tO = tmem + lane_off + uint32_t(2 * BN + w * BN);
+        const uint32_t tS = tmem + lane_off + TM_S + uint32_t(half * HALF);
+        const uint32_t tO = tmem + lane_off + TM_O;
+        const uint32_t tP = tmem + lane_off + TM_P + uint32_t(half * (HALF / 4));
+        // O has DV value columns and 16 copies of l; this thread rescales and
+        // writes [oc0, oc1) of them (multiples of 16).
+        const int ncol = p.DV + 16;
+        const int split = ((ncol / 2) + 15) & ~15;
+        const int oc0 = half ? split : 0;
+        const int oc1 = half ? ncol : split;
+        const uint32_t xm_base = sb + SM_XM + uint32_t(r * 8);
         const float c = p.st->scale[0] * p.st->scale[1] * p.sm_scale * 1.4426950408889634f;
+        const uint64_t c2 = f32x2_pack(c, c);
         float m_ref = 0.0f;
-        float l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            // S_w(j) complete; so is every P.V of earlier tiles into O_w.
-            ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + w), j & 1, abort_flag, err));
+            ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL), j & 1, abort_flag, err));
             if (!ok) break;
             tc_fence_after();
             uint32_t s0[32], s1[32], s2[32], s3[32];
@@ -271,6 +335,10 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             reg_fence32(s1);
             reg_fence32(s2);
             reg_fence32(s3);
+            // S(j) is in registers: the tensor core may overwrite it with S(j+1).
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SFREE));
 
             float sf[128];
 #pragma unroll
@@ -280,8 +348,8 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 sf[64 + i] = __uint_as_float(s2[i]);
                 sf[96 + i] = __uint_as_float(s3[i]);
             }
-            const int key0 = kbase + j * BN;
-            if (key0 < seg_s || key0 + BN > seg_e) {
+            const int key0 = kbase + j * BN + half * HALF;
+            if (key0 < seg_s || key0 + HALF > seg_e) {
 #pragma unroll
                 for (int i = 0; i < 128; ++i) {
                     const int key = key0 + i;
@@ -296,50 +364,49 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
                 mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
             }
-            const float xmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+            // Row maximum over both key halves (the partner thread holds the other).
+            const float pmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            const uint32_t xpar = uint32_t(j & 1) * (2 * BM * 8);
+            uint32_t omax = 0;
+            ok = __all_sync(0xFFFFFFFFu,
+                            pair_swap(xm_base + xpar + uint32_t(half * BM * 8),
+                                      xm_base + xpar + uint32_t((1 - half) * BM * 8),
+                                      __float_as_uint(pmax), uint32_t(j), omax, abort_flag, err));
+            if (!ok) break;
+            const float xmax = fmaxf(pmax, __uint_as_float(omax)) * c;
             float oscale = 1.0f;
             bool need = false;
             if (j == 0) {
                 m_ref = ceilf(xmax);
-            } else if (xmax > m_ref) {
+            } else if (xmax > m_ref + SLACK) {
                 const float mnew = ceilf(xmax);
                 oscale = exp2_int(m_ref - mnew);
-                l *= oscale;
                 m_ref = mnew;
                 need = true;
             }
             const float bias = PSHIFT - m_ref;
+            const uint64_t b2 = f32x2_pack(bias, bias);
 
-            // P' = E4M3(2^(x - m_ref + 8)), four keys per 32-bit word, and the
-            // row sum of those same rounded values (E4M3 -> f16 exact, f16x2
-            // adds over 16 keys, fp32 across), so the weights applied to V sum
-            // to one.
+            // P' = E4M3(2^(x - m_ref + 8)), four keys per 32-bit word.
             uint32_t pk[32];
-            float ls = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = ch * 16 + q * 4;
-                    pk[ch * 4 + q] = cvt_e4m3x4(ex2_approx(fmaf(sf[i + 0], c, bias)),
-                                                ex2_approx(fmaf(sf[i + 1], c, bias)),
-                                                ex2_approx(fmaf(sf[i + 2], c, bias)),
-                                                ex2_approx(fmaf(sf[i + 3], c, bias)));
-                }
-                const uint32_t* wd = pk + ch * 4;
-                const uint32_t a = hadd2(e4m3x2_to_f16x2(wd[0] & 0xFFFFu), e4m3x2_to_f16x2(wd[0] >> 16));
-                const uint32_t b = hadd2(e4m3x2_to_f16x2(wd[1] & 0xFFFFu), e4m3x2_to_f16x2(wd[1] >> 16));
-                const uint32_t d = hadd2(e4m3x2_to_f16x2(wd[2] & 0xFFFFu), e4m3x2_to_f16x2(wd[2] >> 16));
-                const uint32_t e = hadd2(e4m3x2_to_f16x2(wd[3] & 0xFFFFu), e4m3x2_to_f16x2(wd[3] >> 16));
-                const float2 f = f16x2_to_float2(hadd2(hadd2(a, b), hadd2(d, e)));
-                ls += f.x + f.y;
+            for (int q = 0; q < 32; ++q) {
+                float y0, y1, y2, y3;
+                f32x2_unpack(ffma2(f32x2_pack(sf[4 * q], sf[4 * q + 1]), c2, b2), y0, y1);
+                f32x2_unpack(ffma2(f32x2_pack(sf[4 * q + 2], sf[4 * q + 3]), c2, b2), y2, y3);
+                pk[q] = cvt_e4m3x4(ex2_approx(y0), ex2_approx(y1), ex2_approx(y2), ex2_approx(y3));
             }
-            l += ls;
 
+            if (j > 0) {
+                // P(j-1) V_{j-1} complete: P's columns are free and O (with l)
+                // is final up to tile j-1 (needed before a rescale).
+                ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL), (j - 1) & 1, abort_flag, err));
+                if (!ok) break;
+                tc_fence_after();
+            }
             if (__any_sync(0xFFFFFFFFu, need)) {
-                // O_w holds every P.V before tile j (complete, see above).
                 const uint64_t s2v = f32x2_pack(oscale, oscale);
-                for (int cc = 0; cc < p.DV; cc += 16) {
+                for (int cc = oc0; cc < oc1; cc += 16) {
                     uint32_t o[16];
                     tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
                     tmem_ld_wait16(o);
@@ -354,19 +421,23 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tmem_st_32x32b_x16(tO + uint32_t(cc), o);
                 }
             }
-            // P row into the first 32 columns of this row's S region.
-            tmem_st_32x32b_x32(tS, pk);
+            // This half of the P row: 128 keys in 32 columns.
+            tmem_st_32x32b_x32(tP, pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PFULL + w));
+            if (lane == 0) mbar_arrive(BAR(B_PFULL));
         }
-        if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OREADY + w), 0, abort_flag, err));
+        if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL), (nkv - 1) & 1, abort_flag, err));
         if (ok) {
             tc_fence_after();
-            const float oscale = p.st->scale[2] / l;
+            uint32_t lv[16];
+            tmem_ld_32x32b_x16(tO + uint32_t(p.DV), lv);
+            tmem_ld_wait16(lv);
+            const float oscale = p.st->scale[2] / __uint_as_float(lv[0]);
             uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
-            for (int cc = 0; cc < p.DV; cc += 16) {
+            const int oend = oc1 < p.DV ? oc1 : p.DV;
+            for (int cc = oc0; cc < oend; cc += 16) {
                 uint32_t o[16];
                 tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
                 tmem_ld_wait16(o);
@@ -398,7 +469,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 // Work list: segments sorted longest first (when there are at most 2048),
-// items per segment = ceil(L / 256) * H, prefix sums over the sorted order.
+// items per segment = ceil(L / rows_per_item) * H, prefix sums over the sorted order.
 __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T, int H,
                                  int rows_per_item, WsHeader* ws, int32_t* order, int32_t* prefix) {
     __shared__ int bad;
@@ -499,7 +570,7 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
         !make_map_3d_u8(&mk, k8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
                         uint64_t(H) * Dp, 128, 1, BN) ||
         !make_map_3d_u8(&mv, v8t, uint64_t(Tv), uint64_t(Dp), uint64_t(H), uint64_t(Tv),
-                        uint64_t(Tv) * Dp, BN, uint32_t(DV), 1))
+                        uint64_t(Tv) * Dp, HALF, uint32_t(DV), 1))
         return VITFP8_ERR_CUDA;
 
     if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, ws, s) != cudaSuccess) return VITFP8_ERR_CUDA;

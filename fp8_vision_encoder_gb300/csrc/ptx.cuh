@@ -38,6 +38,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same, letting the hardware suspend the thread for up to `ns` nanoseconds
+// while the phase is incomplete (it resumes as soon as the phase completes),
+// so a waiting warp polls rarely instead of spinning on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- proxies
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor core) before a later synchronisation.
