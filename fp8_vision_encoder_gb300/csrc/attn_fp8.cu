@@ -15,10 +15,11 @@
 //               -> F32) into tensor memory: S(j+1) = Q K_{j+1}^T (N = 256) as
 //               soon as the softmax has read S(j), and O += P(j) V_j (P read
 //               from TMEM) as soon as P(j) is written.
-//   warps 0-7   softmax, two threads per query row: warp w and warp w + 4 read
-//               the same TMEM lanes (rows 32(w%4) ..), warps 0-3 the keys
-//               0..127 of a tile and warps 4-7 the keys 128..255.  The two
-//               halves of a row swap their partial maxima through shared memory.
+//   warps 0-7   softmax: warp w owns the 16 rows 32(w%4) + 16(w/4) .. +15;
+//               two threads of the warp share each row (TMEM access shape
+//               16x32bx2), lanes 0-15 taking the keys 0..127 of a tile and
+//               lanes 16-31 the keys 128..255, and combine their row maxima
+//               with one shuffle.  No warp waits for another inside a tile.
 //
 // TMEM (512 columns): S in 0..255 (fp32, 256 keys), O in 256..399, P in
 // 448..511 (E4M3, four keys per column).  Because P has its own columns, the
@@ -80,8 +81,7 @@ constexpr float SLACK = 0.8f;            // x may exceed m_ref by this: P' <= 2^
 constexpr int SM_Q = 0;
 constexpr int SM_K = SM_Q + QBYTES;
 constexpr int SM_V = SM_K + NST * KBYTES;
-constexpr int SM_XM = SM_V + NST * VBYTES;       // [2 parities][2 halves][128 rows] x 8 B
-constexpr int SM_BAR = SM_XM + 2 * 2 * BM * 8;
+constexpr int SM_BAR = SM_V + NST * VBYTES;
 // barrier indices
 constexpr int B_QFULL = 0;
 constexpr int B_KFULL = 1;
@@ -99,37 +99,9 @@ constexpr int SM_USED = SM_ABORT + 4;
 constexpr int SMEM_BYTES = SM_USED + 1024;  // + slack to align the base to 1024
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 448;
+constexpr int OSPLIT = 80;               // O columns per half-row thread (2 x 80 >= 128 + 16)
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 }  // namespace fa
-
-// Swap one 32-bit value with the partner thread (same row, other key half)
-// through shared memory: the value and a tag are written as one 8-byte word;
-// the partner's word is polled until it carries the same tag.  Bounded like
-// every other wait; false when the CTA aborts or the wait times out.
-__device__ __forceinline__ bool pair_swap(uint32_t mine_addr, uint32_t other_addr, uint32_t value,
-                                          uint32_t tag, uint32_t& other, volatile int* abort_flag,
-                                          int32_t* err) {
-    asm volatile("st.volatile.shared.v2.b32 [%0], {%1, %2};" ::"r"(mine_addr), "r"(value), "r"(tag)
-                 : "memory");
-    const long long t0 = clock64();
-    for (uint32_t it = 0;; ++it) {
-        uint32_t v, t;
-        asm volatile("ld.volatile.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v), "=r"(t) : "r"(other_addr)
-                     : "memory");
-        if (t == tag) {
-            other = v;
-            return true;
-        }
-        if ((it & 15u) == 15u) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > ATTN_WAIT_LIMIT) {
-                *abort_flag = 1;
-                record_error(err, VITFP8_ERR_DEVICE_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
 
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -168,9 +140,6 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Exchange words start with a tag no handshake uses.
-    for (int i = threadIdx.x; i < (SM_BAR - SM_XM) / 4; i += blockDim.x)
-        reinterpret_cast<uint32_t*>(smem + SM_XM)[i] = 0xFFFFFFFFu;
     // Rows DV..DV+15 of every V^T block hold E4M3 1.0 (0x38) for good: the
     // TMA boxes cover rows 0..DV-1 only.  (Uniform bytes: the swizzle does not
     // matter.)  The tensor core reads them through the async proxy.
@@ -302,22 +271,15 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else {
         // ------------------------------------------------ softmax (warps 0..7)
-        const int half = warp >> 2;           // keys half*128 .. half*128+127 of each tile
-        const int sub = warp & 3;             // TMEM lane quarter
-        const int r = sub * 32 + lane;        // row inside the query tile
+        const int half = lane >> 4;           // keys half*128 .. half*128+127 of each tile
+        const int rbase = 32 * (warp & 3) + 16 * (warp >> 2);
+        const int r = rbase + (lane & 15);    // row inside the query tile
         const int qrow = q0 + r;              // packed token index of this row
         const bool row_valid = qrow < seg_e;
-        const uint32_t lane_off = uint32_t(sub * 32) << 16;
-        const uint32_t tS = tmem + lane_off + TM_S + uint32_t(half * HALF);
+        const uint32_t lane_off = uint32_t(rbase) << 16;
+        const uint32_t tS = tmem + lane_off + TM_S;
         const uint32_t tO = tmem + lane_off + TM_O;
-        const uint32_t tP = tmem + lane_off + TM_P + uint32_t(half * (HALF / 4));
-        // O has DV value columns and 16 copies of l; this thread rescales and
-        // writes [oc0, oc1) of them (multiples of 16).
-        const int ncol = p.DV + 16;
-        const int split = ((ncol / 2) + 15) & ~15;
-        const int oc0 = half ? split : 0;
-        const int oc1 = half ? ncol : split;
-        const uint32_t xm_base = sb + SM_XM + uint32_t(r * 8);
+        const uint32_t tP = tmem + lane_off + TM_P;
         const float c = p.st->scale[0] * p.st->scale[1] * p.sm_scale * 1.4426950408889634f;
         const uint64_t c2 = f32x2_pack(c, c);
         float m_ref = 0.0f;
@@ -327,10 +289,10 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             uint32_t s0[32], s1[32], s2[32], s3[32];
-            tmem_ld_32x32b_x32(tS + 0, s0);
-            tmem_ld_32x32b_x32(tS + 32, s1);
-            tmem_ld_32x32b_x32(tS + 64, s2);
-            tmem_ld_32x32b_x32(tS + 96, s3);
+            tmem_ld_16x2_x32<HALF>(tS + 0, s0);
+            tmem_ld_16x2_x32<HALF>(tS + 32, s1);
+            tmem_ld_16x2_x32<HALF>(tS + 64, s2);
+            tmem_ld_16x2_x32<HALF>(tS + 96, s3);
             tmem_ld_wait(s0);
             reg_fence32(s1);
             reg_fence32(s2);
@@ -364,16 +326,10 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
                 mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
             }
-            // Row maximum over both key halves (the partner thread holds the other).
-            const float pmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-            const uint32_t xpar = uint32_t(j & 1) * (2 * BM * 8);
-            uint32_t omax = 0;
-            ok = __all_sync(0xFFFFFFFFu,
-                            pair_swap(xm_base + xpar + uint32_t(half * BM * 8),
-                                      xm_base + xpar + uint32_t((1 - half) * BM * 8),
-                                      __float_as_uint(pmax), uint32_t(j), omax, abort_flag, err));
-            if (!ok) break;
-            const float xmax = fmaxf(pmax, __uint_as_float(omax)) * c;
+            // Row maximum over both key halves (lane ^ 16 holds the other half).
+            float pmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, 16));
+            const float xmax = pmax * c;
             float oscale = 1.0f;
             bool need = false;
             if (j == 0) {
@@ -405,10 +361,13 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tc_fence_after();
             }
             if (__any_sync(0xFFFFFFFFu, need)) {
+                // O's DV + 16 columns (values, then copies of l): lanes 0-15
+                // scale columns 0..79, lanes 16-31 columns 80..159 (columns
+                // past DV + 16 are unused TMEM).
                 const uint64_t s2v = f32x2_pack(oscale, oscale);
-                for (int cc = oc0; cc < oc1; cc += 16) {
+                for (int cc = 0; cc < OSPLIT; cc += 16) {
                     uint32_t o[16];
-                    tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
+                    tmem_ld_16x2_x16<OSPLIT>(tO + uint32_t(cc), o);
                     tmem_ld_wait16(o);
 #pragma unroll
                     for (int q = 0; q < 16; q += 2) {
@@ -418,11 +377,11 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         o[q] = __float_as_uint(a0);
                         o[q + 1] = __float_as_uint(a1);
                     }
-                    tmem_st_32x32b_x16(tO + uint32_t(cc), o);
+                    tmem_st_16x2_x16<OSPLIT>(tO + uint32_t(cc), o);
                 }
             }
-            // This half of the P row: 128 keys in 32 columns.
-            tmem_st_32x32b_x32(tP, pk);
+            // This half of the P row: 128 keys in 32 columns (lanes 16-31 at +32).
+            tmem_st_16x2_x32<HALF / 4>(tP, pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -431,15 +390,16 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL), (nkv - 1) & 1, abort_flag, err));
         if (ok) {
             tc_fence_after();
-            uint32_t lv[16];
-            tmem_ld_32x32b_x16(tO + uint32_t(p.DV), lv);
-            tmem_ld_wait16(lv);
-            const float oscale = p.st->scale[2] / __uint_as_float(lv[0]);
+            uint32_t lbits;
+            tmem_ld_16x2_x1<1>(tO + uint32_t(p.DV), lbits);   // both halves: a copy of l
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            asm volatile("" : "+r"(lbits));
+            const float oscale = p.st->scale[2] / __uint_as_float(lbits);
             uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
-            const int oend = oc1 < p.DV ? oc1 : p.DV;
-            for (int cc = oc0; cc < oend; cc += 16) {
+            const int cbase = half * OSPLIT;
+            for (int cc = 0; cc < OSPLIT; cc += 16) {
                 uint32_t o[16];
-                tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
+                tmem_ld_16x2_x16<OSPLIT>(tO + uint32_t(cc), o);
                 tmem_ld_wait16(o);
                 uint32_t pkd[8];
 #pragma unroll
@@ -448,11 +408,12 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                                               __uint_as_float(o[2 * q + 1]) * oscale);
                     pkd[q] = *reinterpret_cast<uint32_t*>(&v2);
                 }
+                const int d0 = cbase + cc;
                 if (row_valid) {
-                    if (cc + 8 <= p.D)
-                        *reinterpret_cast<uint4*>(orow + cc) = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
-                    if (cc + 16 <= p.D)
-                        *reinterpret_cast<uint4*>(orow + cc + 8) = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+                    if (d0 + 8 <= p.D)
+                        *reinterpret_cast<uint4*>(orow + d0) = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+                    if (d0 + 16 <= p.D)
+                        *reinterpret_cast<uint4*>(orow + d0 + 8) = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
                 }
             }
         }
