@@ -11,10 +11,15 @@
 //   warp 8      TMA producer: the Q tile once, then K tiles (256 keys x 128 d)
 //               and V^T tiles (d x 256 keys) through a shared-memory ring
 //               (128-byte swizzle).
-//   warp 9      MMA issuer (one thread), tcgen05.mma kind::f8f6f4 (E4M3 x E4M3
+//   warp 9      S issuer (one thread), tcgen05.mma kind::f8f6f4 (E4M3 x E4M3
 //               -> F32) into tensor memory: S(j+1) = Q K_{j+1}^T (N = 256) as
-//               soon as the softmax has read S(j), and O += P(j) V_j (P read
-//               from TMEM) as soon as P(j) is written.
+//               soon as the softmax has read S(j).
+//   warp 10     P.V issuer (one thread): O += P(j) V_j (P read from TMEM) as
+//               soon as P(j) is written.  One thread needs about as long to
+//               issue an MMA as the tensor core needs to run it; with two
+//               issuers the waits of one overlap the other's MMAs.  The two
+//               streams write different accumulators, so their order in the
+//               tensor pipe does not matter.
 //   warps 0-7   softmax: warp w owns the 16 rows 32(w%4) + 16(w/4) .. +15;
 //               two threads of the warp share each row (TMEM access shape
 //               16x32bx2), lanes 0-15 taking the keys 0..127 of a tile and
@@ -68,9 +73,10 @@ constexpr int ROWS_PER_ITEM = BM;        // queries per work item
 constexpr int BN = 256;                  // keys per tile
 constexpr int HALF = BN / 2;             // keys per softmax thread and tile
 constexpr int NST = 3;                   // K/V pipeline stages
-constexpr int NUM_THREADS = 320;         // 8 softmax warps, TMA warp, MMA warp
+constexpr int NUM_THREADS = 352;         // 8 softmax warps, TMA warp, S and P.V issuers
 constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA = 9;              // S issuer; owns the TMEM allocation
+constexpr int WARP_PV = 10;              // P.V issuer
 constexpr int QBYTES = BM * 128;         // Q tile: 128 rows x 128 bytes
 constexpr int KBYTES = BN * 128;         // K tile: 256 rows x 128 bytes
 constexpr int VBLK = 144 * 128;          // V^T block: up to 128 d-rows + 16 rows of ones, x 128 keys
@@ -86,8 +92,9 @@ constexpr int SM_BAR = SM_V + NST * VBYTES;
 constexpr int B_QFULL = 0;
 constexpr int B_KFULL = 1;
 constexpr int B_VFULL = B_KFULL + NST;
-constexpr int B_KVEMPTY = B_VFULL + NST;
-constexpr int B_SFULL = B_KVEMPTY + NST;   // S(j) complete in TMEM
+constexpr int B_KEMPTY = B_VFULL + NST;    // [NST]: S of the stage's K tile complete
+constexpr int B_VEMPTY = B_KEMPTY + NST;   // [NST]: P.V of the stage's V tile complete
+constexpr int B_SFULL = B_VEMPTY + NST;    // S(j) complete in TMEM
 constexpr int B_SFREE = B_SFULL + 1;       // S(j) read by all 8 softmax warps
 constexpr int B_PFULL = B_SFREE + 1;       // P(j) written by all 8 softmax warps
 constexpr int B_OFULL = B_PFULL + 1;       // P(j) V_j (and every earlier MMA) complete
@@ -154,13 +161,14 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int s = 0; s < NST; ++s) {
             mbar_init(BAR(B_KFULL + s), 1);
             mbar_init(BAR(B_VFULL + s), 1);
-            mbar_init(BAR(B_KVEMPTY + s), 1);
+            mbar_init(BAR(B_KEMPTY + s), 1);
+            mbar_init(BAR(B_VEMPTY + s), 1);
         }
         mbar_init(BAR(B_SFULL), 1);
         mbar_init(BAR(B_SFREE), 8);
         mbar_init(BAR(B_PFULL), 8);
         mbar_init(BAR(B_OFULL), 1);
-        mbar_init(BAR(B_FINAL), 1);
+        mbar_init(BAR(B_FINAL), 2);   // one commit per issuer
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -185,10 +193,14 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             int j = 0;
             for (; j < nkv; ++j) {
                 const int s = j % NST;
-                if (j >= NST && !bwait(BAR(B_KVEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
                 const int key0 = kbase + j * BN;
+                if (j >= NST && !bwait(BAR(B_KEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
                 mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
                 tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, key0);
+                if (j >= NST && !bwait(BAR(B_VEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) {
+                    ++j;   // K_j is in flight: its barrier is drained below
+                    break;
+                }
                 mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
                 tma_load_3d(sb + SM_V + s * VBYTES, &tmV, BAR(B_VFULL + s), key0, 0, h);
                 tma_load_3d(sb + SM_V + s * VBYTES + VBLK, &tmV, BAR(B_VFULL + s), key0 + HALF, 0, h);
@@ -207,17 +219,15 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
     } else if (warp == WARP_MMA) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ S issuer
         if (lane == 0) {
             const uint32_t idS = make_idesc(0, BM, BN);      // 128 x 256 per S product
-            const uint32_t idPV = make_idesc(0, BM, p.DV + 16);   // d columns + the l column block
             // Descriptors are built once: within a 128-byte swizzled row a
-            // 32-byte K step adds 2 to the encoded start address; a stage or a
-            // block adds its byte offset / 16.
+            // 32-byte K step adds 2 to the encoded start address; a stage
+            // adds its byte offset / 16.
             const uint64_t dQ = sw128_kmajor_desc(sb + SM_Q);
             const uint64_t dK0 = sw128_kmajor_desc(sb + SM_K);
-            const uint64_t dV0 = sw128_kmajor_desc(sb + SM_V);
-            const uint32_t tS = tmem + TM_S, tO = tmem + TM_O, tP = tmem + TM_P;
+            const uint32_t tS = tmem + TM_S;
             const int KS = p.KS;
             auto issue_S = [&](int s) {
                 const uint64_t dk = dK0 + uint64_t(s * (KBYTES >> 4));
@@ -229,6 +239,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         umma_f8(tS, dQ + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
                 }
                 tc_commit(BAR(B_SFULL));
+                tc_commit(BAR(B_KEMPTY + s));
             };
             bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
                       bwait(BAR(B_KFULL + 0), 0, abort_flag, err);
@@ -236,29 +247,14 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tc_fence_after();
                 issue_S(0);
             }
-            int s = 0, s1 = 1 % NST;
-            uint32_t ph = 0, ph1 = NST == 1 ? 1u : 0u;
-            for (int j = 0; ok && j < nkv; ++j) {
-                if (j + 1 < nkv) {
-                    // S(j+1) as soon as K_{j+1} is in and every softmax warp has read S(j).
-                    if (!(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
-                    if (!(ok = bwait(BAR(B_SFREE), j & 1, abort_flag, err))) break;
-                    tc_fence_after();
-                    issue_S(s1);
-                }
-                // O += P(j) V_j: 256 keys in 8 steps of 32, keys 0..127 from
-                // V^T block 0 and P columns 0..31, keys 128..255 from block 1
-                // and P columns 32..63.
-                if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
-                if (!(ok = bwait(BAR(B_PFULL), j & 1, abort_flag, err))) break;
+            int s1 = 1 % NST;
+            uint32_t ph1 = NST == 1 ? 1u : 0u;
+            for (int j = 0; ok && j + 1 < nkv; ++j) {
+                // S(j+1) as soon as K_{j+1} is in and every softmax warp has read S(j).
+                if (!(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
+                if (!(ok = bwait(BAR(B_SFREE), j & 1, abort_flag, err))) break;
                 tc_fence_after();
-                const uint64_t dv = dV0 + uint64_t(s * (VBYTES >> 4));
-                umma_f8_ts_k4(tO, tP, dv, idPV, j > 0 ? 1u : 0u);
-                umma_f8_ts_k4(tO, tP + 32u, dv + uint64_t(VBLK >> 4), idPV, 1u);
-                tc_commit(BAR(B_OFULL));
-                tc_commit(BAR(B_KVEMPTY + s));
-                s = s1;
-                ph = ph1;
+                issue_S(s1);
                 if (++s1 == NST) {
                     s1 = 0;
                     ph1 ^= 1u;
@@ -269,7 +265,37 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int spin = 0; spin < (1 << 24); ++spin)
                 if (mbar_try_wait(BAR(B_FINAL), 0)) break;
         }
-    } else {
+    } else if (warp == WARP_PV) {
+        // ------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            const uint32_t idPV = make_idesc(0, BM, p.DV + 16);   // d columns + the l column block
+            const uint64_t dV0 = sw128_kmajor_desc(sb + SM_V);
+            const uint32_t tO = tmem + TM_O, tP = tmem + TM_P;
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int j = 0; ok && j < nkv; ++j) {
+                // O += P(j) V_j: 256 keys in 8 steps of 32, keys 0..127 from
+                // V^T block 0 and P columns 0..31, keys 128..255 from block 1
+                // and P columns 32..63.
+                if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
+                if (!(ok = bwait(BAR(B_PFULL), j & 1, abort_flag, err))) break;
+                tc_fence_after();
+                const uint64_t dv = dV0 + uint64_t(s * (VBYTES >> 4));
+                umma_f8_ts_k4(tO, tP, dv, idPV, j > 0 ? 1u : 0u);
+                umma_f8_ts_k4(tO, tP + 32u, dv + uint64_t(VBLK >> 4), idPV, 1u);
+                tc_commit(BAR(B_OFULL));
+                tc_commit(BAR(B_VEMPTY + s));
+                if (++s == NST) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            tc_commit(BAR(B_FINAL));
+            for (int spin = 0; spin < (1 << 24); ++spin)
+                if (mbar_try_wait(BAR(B_FINAL), 0)) break;
+        }
+    } else if (warp < 8) {
         // ------------------------------------------------ softmax (warps 0..7)
         const int half = lane >> 4;           // keys half*128 .. half*128+127 of each tile
         const int rbase = 32 * (warp & 3) + 16 * (warp >> 2);
