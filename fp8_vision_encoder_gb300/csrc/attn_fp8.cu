@@ -391,20 +391,33 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // scale columns 0..79, lanes 16-31 columns 80..159 (columns
                 // past DV + 16 are unused TMEM).
                 const uint64_t s2v = f32x2_pack(oscale, oscale);
-                for (int cc = 0; cc < OSPLIT; cc += 16) {
-                    uint32_t o[16];
-                    tmem_ld_16x2_x16<OSPLIT>(tO + uint32_t(cc), o);
-                    tmem_ld_wait16(o);
+                uint32_t oa[32], ob[32], oc[16];
+                tmem_ld_16x2_x32<OSPLIT>(tO + 0u, oa);
+                tmem_ld_16x2_x32<OSPLIT>(tO + 32u, ob);
+                tmem_ld_16x2_x16<OSPLIT>(tO + 64u, oc);
+                tmem_ld_wait(oa);
+                reg_fence32(ob);
+                reg_fence16(oc);
 #pragma unroll
-                    for (int q = 0; q < 16; q += 2) {
-                        float a0, a1;
-                        f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(o[q]), __uint_as_float(o[q + 1])), s2v),
-                                     a0, a1);
-                        o[q] = __float_as_uint(a0);
-                        o[q + 1] = __float_as_uint(a1);
-                    }
-                    tmem_st_16x2_x16<OSPLIT>(tO + uint32_t(cc), o);
+                for (int q = 0; q < 32; q += 2) {
+                    float a0, a1;
+                    f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(oa[q]), __uint_as_float(oa[q + 1])), s2v), a0, a1);
+                    oa[q] = __float_as_uint(a0);
+                    oa[q + 1] = __float_as_uint(a1);
+                    f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(ob[q]), __uint_as_float(ob[q + 1])), s2v), a0, a1);
+                    ob[q] = __float_as_uint(a0);
+                    ob[q + 1] = __float_as_uint(a1);
                 }
+#pragma unroll
+                for (int q = 0; q < 16; q += 2) {
+                    float a0, a1;
+                    f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(oc[q]), __uint_as_float(oc[q + 1])), s2v), a0, a1);
+                    oc[q] = __float_as_uint(a0);
+                    oc[q + 1] = __float_as_uint(a1);
+                }
+                tmem_st_16x2_x32<OSPLIT>(tO + 0u, oa);
+                tmem_st_16x2_x32<OSPLIT>(tO + 32u, ob);
+                tmem_st_16x2_x16<OSPLIT>(tO + 64u, oc);
             }
             // This half of the P row: 128 keys in 32 columns (lanes 16-31 at +32).
             tmem_st_16x2_x32<HALF / 4>(tP, pk);
