@@ -314,15 +314,18 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL), j & 1, abort_flag, err));
             if (!ok) break;
             tc_fence_after();
-            uint32_t s0[32], s1[32], s2[32], s3[32];
-            tmem_ld_16x2_x32<HALF>(tS + 0, s0);
-            tmem_ld_16x2_x32<HALF>(tS + 32, s1);
-            tmem_ld_16x2_x32<HALF>(tS + 64, s2);
-            tmem_ld_16x2_x32<HALF>(tS + 96, s3);
-            tmem_ld_wait(s0);
-            reg_fence32(s1);
-            reg_fence32(s2);
-            reg_fence32(s3);
+            // The loads also return each 32-key chunk's maximum (tcgen05.ld.red).
+            float s0[32], s1[32], s2[32], s3[32];
+            float m0, m1, m2, m3;
+            tmem_ld_16x2_x32_max<HALF>(tS + 0, s0, m0);
+            tmem_ld_16x2_x32_max<HALF>(tS + 32, s1, m1);
+            tmem_ld_16x2_x32_max<HALF>(tS + 64, s2, m2);
+            tmem_ld_16x2_x32_max<HALF>(tS + 96, s3, m3);
+            tmem_ld_wait_f32(s0);
+            reg_fence_f32(s1);
+            reg_fence_f32(s2);
+            reg_fence_f32(s3);
+            asm volatile("" : "+f"(m0), "+f"(m1), "+f"(m2), "+f"(m3));
             // S(j) is in registers: the tensor core may overwrite it with S(j+1).
             tc_fence_before();
             __syncwarp();
@@ -331,29 +334,32 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             float sf[128];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                sf[i] = __uint_as_float(s0[i]);
-                sf[32 + i] = __uint_as_float(s1[i]);
-                sf[64 + i] = __uint_as_float(s2[i]);
-                sf[96 + i] = __uint_as_float(s3[i]);
+                sf[i] = s0[i];
+                sf[32 + i] = s1[i];
+                sf[64 + i] = s2[i];
+                sf[96 + i] = s3[i];
             }
             const int key0 = kbase + j * BN + half * HALF;
+            float pmax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
             if (key0 < seg_s || key0 + HALF > seg_e) {
+                // First or last tile: keys outside the segment are masked, and
+                // the maximum is taken over the keys left.
 #pragma unroll
                 for (int i = 0; i < 128; ++i) {
                     const int key = key0 + i;
                     if (key < seg_s || key >= seg_e) sf[i] = -INFINITY;
                 }
-            }
-            float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
+                float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
 #pragma unroll
-            for (int i = 4; i < 128; i += 8) {
-                mx0 = fmax3(mx0, sf[i], sf[i + 1]);
-                mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
-                mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
-                mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
+                for (int i = 4; i < 128; i += 8) {
+                    mx0 = fmax3(mx0, sf[i], sf[i + 1]);
+                    mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
+                    mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
+                    mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
+                }
+                pmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
             }
             // Row maximum over both key halves (lane ^ 16 holds the other half).
-            float pmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
             pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, 16));
             const float xmax = pmax * c;
             float oscale = 1.0f;

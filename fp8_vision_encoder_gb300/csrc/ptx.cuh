@@ -242,12 +242,37 @@ __device__ __forceinline__ void tmem_ld_16x2_x32(uint32_t taddr, uint32_t (&r)[3
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr), "n"(SPLIT));
 }
+// Same shape, loading fp32 values and returning in `mx` the maximum of this
+// thread's 32 loaded values (tcgen05.ld.red, max reduction done by the load).
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld_16x2_x32_max(uint32_t taddr, float (&r)[32], float& mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.16x32bx2.x32.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33], %34;"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31]), "=f"(mx)
+        : "r"(taddr), "n"(SPLIT));
+}
+// Pins 32 fp32 registers after tcgen05.wait::ld (their loads are complete).
+__device__ __forceinline__ void tmem_ld_wait_f32(float (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" : "+f"(r[0]), "+f"(r[1]), "+f"(r[2]), "+f"(r[3]), "+f"(r[4]), "+f"(r[5]), "+f"(r[6]), "+f"(r[7]), "+f"(r[8]), "+f"(r[9]), "+f"(r[10]), "+f"(r[11]), "+f"(r[12]), "+f"(r[13]), "+f"(r[14]), "+f"(r[15]), "+f"(r[16]), "+f"(r[17]), "+f"(r[18]), "+f"(r[19]), "+f"(r[20]), "+f"(r[21]), "+f"(r[22]), "+f"(r[23]), "+f"(r[24]), "+f"(r[25]), "+f"(r[26]), "+f"(r[27]), "+f"(r[28]), "+f"(r[29]), "+f"(r[30]), "+f"(r[31]) : : "memory");
+}
+__device__ __forceinline__ void reg_fence_f32(float (&r)[32]) {
+    asm volatile("" : "+f"(r[0]), "+f"(r[1]), "+f"(r[2]), "+f"(r[3]), "+f"(r[4]), "+f"(r[5]), "+f"(r[6]), "+f"(r[7]), "+f"(r[8]), "+f"(r[9]), "+f"(r[10]), "+f"(r[11]), "+f"(r[12]), "+f"(r[13]), "+f"(r[14]), "+f"(r[15]), "+f"(r[16]), "+f"(r[17]), "+f"(r[18]), "+f"(r[19]), "+f"(r[20]), "+f"(r[21]), "+f"(r[22]), "+f"(r[23]), "+f"(r[24]), "+f"(r[25]), "+f"(r[26]), "+f"(r[27]), "+f"(r[28]), "+f"(r[29]), "+f"(r[30]), "+f"(r[31]));
+}
 template <int SPLIT>
 __device__ __forceinline__ void tmem_ld_16x2_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr), "n"(SPLIT));
+}
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld_16x2_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
         : "r"(taddr), "n"(SPLIT));
 }
 template <int SPLIT>
@@ -270,6 +295,24 @@ __device__ __forceinline__ void tmem_st_16x2_x16(uint32_t taddr, const uint32_t 
         "[%16], %17, {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15};"
         :
         : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(taddr), "n"(SPLIT)
+        : "memory");
+}
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st_16x2_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x8.b32 "
+        "[%8], %9, {%0,%1,%2,%3,%4,%5,%6,%7};"
+        :
+        : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(taddr), "n"(SPLIT)
+        : "memory");
+}
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st_16x2_x4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x4.b32 "
+        "[%4], %5, {%0,%1,%2,%3};"
+        :
+        : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(taddr), "n"(SPLIT)
         : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
