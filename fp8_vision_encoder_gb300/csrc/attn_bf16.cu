@@ -2,21 +2,27 @@
 //
 // "FP8 ViT Encoder Attention", Performance: every table compares the FP8 path
 // with BF16 attention on the same workload.  This kernel is the BF16 column,
-// built like the FP8 kernel so the two differ only in the arithmetic: the same
-// work items (256 queries of one segment and head), the same warp roles (TMA
-// warp, one MMA issuer, two softmax warpgroups), P kept in tensor memory over
-// S, S of the next key tile issued right after each tile's P.V.
+// built like the FP8 kernel so that the two differ in the arithmetic and in
+// what the arithmetic forces:
 //
-// Differences from the FP8 kernel:
-//   * tcgen05.mma kind::f16 (BF16 x BF16 -> F32), K = 16 per instruction;
-//   * Q, K and V are read straight from the bf16 [T][H][D] tensors; a 128-d
-//     row is two 128-byte swizzled blocks of 64 elements;
-//   * V is the B operand in MN-major form (d contiguous), so no transpose;
-//   * P = bf16(2^(x - m_ref)) occupies 64 TMEM columns; as in the FP8 kernel
-//     the row sum adds the rounded weights, so the weights applied to V sum
-//     to one; two K/V stages (the bf16 tiles are twice as large).
+//   * one CTA: one query tile of 128 rows against every key tile of its
+//     segment; warp 8 loads (TMA), warp 9 issues S = Q K^T, warp 10 issues
+//     O += P V, warps 0-7 run the softmax with two threads of one warp per row
+//     (TMEM access shape 16x32bx2) and the row maximum returned by the score
+//     load (tcgen05.ld.red);
+//   * tcgen05.mma kind::f16 (BF16 x BF16 -> F32), K = 16 per instruction, so
+//     a key tile of 128 costs the tensor core as much as 256 keys in FP8: the
+//     key tiles are 128 wide, and S and P are both double-buffered in TMEM
+//     (S 2 x 128 columns, O 128, P 2 x 64: bf16 pairs), which lets S(j+1) run
+//     while the softmax works on S(j) and decouples the softmax warps;
+//   * Q, K and V are read straight from the bf16 [T][H][D] tensors, a 128-d
+//     row being two 128-byte swizzled blocks of 64 elements; V is the B
+//     operand in MN-major form (d contiguous), so no transpose is needed;
+//   * P = bf16(2^(x - m_ref)) and l is the fp32 sum of those rounded weights
+//     (the weights applied to V sum to one), computed by the softmax threads.
+//
 // Key tiles start at the segment start (no alignment constraint on the token
-// coordinate here); keys outside the segment are masked.
+// coordinate); keys outside the segment are masked.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -28,35 +34,42 @@
 namespace vitfp8 {
 
 namespace fb {
-constexpr int BM = 128;
-constexpr int NQT = 2;
-constexpr int ROWS_PER_ITEM = BM * NQT;
-constexpr int BN = 128;
-constexpr int NST = 2;
-constexpr int NUM_THREADS = 320;
+constexpr int BM = 128;                  // query rows per CTA
+constexpr int ROWS_PER_ITEM = BM;
+constexpr int BN = 128;                  // keys per tile
+constexpr int HALF = BN / 2;             // keys per softmax thread and tile
+constexpr int NST = 3;                   // K/V pipeline stages
+constexpr int NUM_THREADS = 352;         // 8 softmax warps, TMA warp, S and P.V issuers
 constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;
-constexpr int BLK = 128 * 128;     // one 128-row x 128-byte swizzled block (64 bf16 per row)
-constexpr int TILE = 2 * BLK;      // 128 rows x 128 bf16 = two blocks along d
+constexpr int WARP_MMA = 9;              // S issuer; owns the TMEM allocation
+constexpr int WARP_PV = 10;              // P.V issuer
+constexpr int BLK = 128 * 128;           // one 128-row x 128-byte swizzled block (64 bf16 per row)
+constexpr int TILE = 2 * BLK;            // 128 rows x 128 bf16 = two blocks along d
 
-constexpr int SM_Q = 0;                      // [NQT] tiles
-constexpr int SM_K = SM_Q + NQT * TILE;      // [NST]
-constexpr int SM_V = SM_K + NST * TILE;      // [NST]: V rows are keys, blocks split d
+constexpr int SM_Q = 0;
+constexpr int SM_K = SM_Q + TILE;
+constexpr int SM_V = SM_K + NST * TILE;  // V rows are keys, blocks split d
 constexpr int SM_BAR = SM_V + NST * TILE;
 constexpr int B_QFULL = 0;
 constexpr int B_KFULL = 1;
 constexpr int B_VFULL = B_KFULL + NST;
-constexpr int B_KVEMPTY = B_VFULL + NST;
-constexpr int B_SFULL = B_KVEMPTY + NST;
-constexpr int B_PFULL = B_SFULL + NQT;
-constexpr int B_OREADY = B_PFULL + NQT;
-constexpr int B_FINAL = B_OREADY + NQT;
+constexpr int B_KEMPTY = B_VFULL + NST;
+constexpr int B_VEMPTY = B_KEMPTY + NST;
+constexpr int B_SFULL = B_VEMPTY + NST;  // [2]: S(j) in buffer j%2 complete
+constexpr int B_SFREE = B_SFULL + 2;     // [2]: S(j) read by all 8 softmax warps
+constexpr int B_PFULL = B_SFREE + 2;     // [2]: P(j) written by all 8 softmax warps
+constexpr int B_OFULL = B_PFULL + 2;     // [2]: P(j) V_j (and every earlier P.V) complete
+constexpr int B_FINAL = B_OFULL + 2;
 constexpr int NBAR = B_FINAL + 1;
 constexpr int SM_TMEMPTR = SM_BAR + NBAR * 8;
 constexpr int SM_ABORT = SM_TMEMPTR + 4;
 constexpr int SM_USED = SM_ABORT + 4;
 constexpr int SMEM_BYTES = SM_USED + 1024;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;   // S and P: buffer b at + b * 128 / + b * 64
+constexpr int OSPLIT = 64;               // O columns per half-row thread
+constexpr float RESCALE_AT = 8.0f;       // the reference moves when P would exceed 2^8
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 }  // namespace fb
 
 __global__ void __launch_bounds__(fb::NUM_THREADS, 1)
@@ -67,7 +80,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int total = p.ws->total_items;
     if (item >= total) return;
 
-    int lo = 0, hi = p.nseq - 1;
+    int lo = 0, hi = p.nseq - 1;  // largest pos with prefix[pos] <= item
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (p.prefix[mid] <= item) lo = mid; else hi = mid - 1;
@@ -99,14 +112,16 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int s = 0; s < NST; ++s) {
             mbar_init(BAR(B_KFULL + s), 1);
             mbar_init(BAR(B_VFULL + s), 1);
-            mbar_init(BAR(B_KVEMPTY + s), 1);
+            mbar_init(BAR(B_KEMPTY + s), 1);
+            mbar_init(BAR(B_VEMPTY + s), 1);
         }
-        for (int w = 0; w < NQT; ++w) {
-            mbar_init(BAR(B_SFULL + w), 1);
-            mbar_init(BAR(B_PFULL + w), 4);
-            mbar_init(BAR(B_OREADY + w), 1);
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(BAR(B_SFULL + b2), 1);
+            mbar_init(BAR(B_SFREE + b2), 8);
+            mbar_init(BAR(B_PFULL + b2), 8);
+            mbar_init(BAR(B_OFULL + b2), 1);
         }
-        mbar_init(BAR(B_FINAL), 1);
+        mbar_init(BAR(B_FINAL), 2);   // one commit per issuer
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -120,30 +135,34 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEMPTR);
 
     if (warp == WARP_TMA) {
+        // ------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             // d 64..127 only when the head has them (a box wholly past D is skipped)
             const int nblk = p.D > 64 ? 2 : 1;
-            mbar_arrive_expect_tx(BAR(B_QFULL), NQT * nblk * BLK);
-            for (int w = 0; w < NQT; ++w)
-                for (int blk = 0; blk < nblk; ++blk)
-                    tma_load_3d(sb + SM_Q + w * TILE + blk * BLK, &tmQ, BAR(B_QFULL), blk * 64, h,
-                                q0 + w * BM);
+            mbar_arrive_expect_tx(BAR(B_QFULL), nblk * BLK);
+            for (int blk = 0; blk < nblk; ++blk)
+                tma_load_3d(sb + SM_Q + blk * BLK, &tmQ, BAR(B_QFULL), blk * 64, h, q0);
             int j = 0;
             for (; j < nkv; ++j) {
                 const int s = j % NST;
-                if (j >= NST && !bwait(BAR(B_KVEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
                 const int key0 = kbase + j * BN;
+                if (j >= NST && !bwait(BAR(B_KEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
                 mbar_arrive_expect_tx(BAR(B_KFULL + s), nblk * BLK);
                 for (int blk = 0; blk < nblk; ++blk)
                     tma_load_3d(sb + SM_K + s * TILE + blk * BLK, &tmK, BAR(B_KFULL + s), blk * 64, h, key0);
+                if (j >= NST && !bwait(BAR(B_VEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) {
+                    ++j;   // K_j is in flight: its barrier is drained below
+                    break;
+                }
                 mbar_arrive_expect_tx(BAR(B_VFULL + s), nblk * BLK);
                 for (int blk = 0; blk < nblk; ++blk)
                     tma_load_3d(sb + SM_V + s * TILE + blk * BLK, &tmV, BAR(B_VFULL + s), blk * 64, h, key0);
             }
             if (*abort_flag) {
+                // Let the copies this thread started land before the CTA exits.
                 bwait(BAR(B_QFULL), 0, abort_flag, err);
                 for (int jj = (j > NST ? j - NST : 0); jj < j; ++jj) {
                     const int s = jj % NST;
@@ -156,179 +175,218 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
         }
     } else if (warp == WARP_MMA) {
+        // ------------------------------------------------ S issuer
         if (lane == 0) {
             const uint32_t idS = make_idesc(1, BM, BN);
-            const uint32_t idPV = make_idesc_bmn(1, BM, p.DV);
-            const uint64_t dQ[NQT] = {sw128_kmajor_desc(sb + SM_Q), sw128_kmajor_desc(sb + SM_Q + TILE)};
+            const uint64_t dQ = sw128_kmajor_desc(sb + SM_Q);
             const uint64_t dK0 = sw128_kmajor_desc(sb + SM_K);
-            // V: MN-major (d contiguous), 64-element d groups BLK apart, 8-key
-            // groups 1024 bytes apart; one K step (16 keys) advances 2048 bytes.
-            const uint64_t dV0 = sw128_mnmajor_desc(sb + SM_V, BLK, 1024);
             const int KS = (p.D + 15) / 16;  // 16-wide K steps over d
-            auto issue_S = [&](int w, int s) {
+            bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int t = 0; ok && t < nkv; ++t) {
+                // S(t) into buffer t % 2 once K_t is in and S(t-2) has been read.
+                const int sbuf = t & 1;
+                if (!(ok = bwait(BAR(B_KFULL + s), ph, abort_flag, err))) break;
+                if (t >= 2 && !(ok = bwait(BAR(B_SFREE + sbuf), ((t - 2) >> 1) & 1, abort_flag, err))) break;
+                tc_fence_after();
                 const uint64_t dk = dK0 + uint64_t(s * (TILE >> 4));
-                const uint32_t dS = tmem + uint32_t(w * 128);
+                const uint32_t dS = tmem + TM_S + uint32_t(sbuf * BN);
                 for (int kk = 0; kk < KS; ++kk) {
                     // step kk: block kk / 4, 32-byte offset (kk % 4) inside the row
                     const uint64_t off = uint64_t((kk >> 2) * (BLK >> 4) + 2 * (kk & 3));
-                    umma_bf16(dS, dQ[w] + off, dk + off, idS, kk > 0 ? 1u : 0u);
+                    umma_bf16(dS, dQ + off, dk + off, idS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(BAR(B_SFULL + w));
-            };
-            bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
-                      bwait(BAR(B_KFULL + 0), 0, abort_flag, err);
-            if (ok) {
-                tc_fence_after();
-                issue_S(0, 0);
-                issue_S(1, 0);
+                tc_commit(BAR(B_SFULL + sbuf));
+                tc_commit(BAR(B_KEMPTY + s));
+                if (++s == NST) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
+            // Every MMA issued above has completed before TMEM is released.
+            tc_commit(BAR(B_FINAL));
+            for (int spin = 0; spin < (1 << 24); ++spin)
+                if (mbar_try_wait(BAR(B_FINAL), 0)) break;
+        }
+    } else if (warp == WARP_PV) {
+        // ------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            const uint32_t idPV = make_idesc_bmn(1, BM, p.DV);
+            // V: MN-major (d contiguous), 64-element d groups BLK apart, 8-key
+            // groups 1024 bytes apart; one K step (16 keys) advances 2048 bytes.
+            const uint64_t dV0 = sw128_mnmajor_desc(sb + SM_V, BLK, 1024);
+            const uint32_t tO = tmem + TM_O;
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
             for (int j = 0; ok && j < nkv; ++j) {
-                const int s = j % NST;
-                const uint32_t ph = (j / NST) & 1;
-                const bool nxt = j + 1 < nkv;
-                const int s1 = (j + 1) % NST;
-                const uint32_t ph1 = ((j + 1) / NST) & 1;
+                const int pb = j & 1;
                 if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
-                if (nxt && !(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
+                if (!(ok = bwait(BAR(B_PFULL + pb), (j >> 1) & 1, abort_flag, err))) break;
+                tc_fence_after();
+                const uint32_t aP = tmem + TM_P + uint32_t(pb * (BN / 2));
                 const uint64_t dv = dV0 + uint64_t(s * (TILE >> 4));
-                for (int w = 0; w < NQT; ++w) {
-                    if (!(ok = bwait(BAR(B_PFULL + w), j & 1, abort_flag, err))) break;
-                    tc_fence_after();
-                    const uint32_t dO = tmem + uint32_t(256 + w * 128);
-                    const uint32_t aP = tmem + uint32_t(w * 128);
-                    // K = 128 keys in 8 steps of 16: P columns + 8, V + 2048 bytes
+                // K = 128 keys in 8 steps of 16: P columns + 8, V + 2048 bytes
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        umma_bf16_ts(dO, aP + uint32_t(8 * kk), dv + uint64_t(kk * (2048 >> 4)), idPV,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
-                    if (nxt)
-                        issue_S(w, s1);
-                    else
-                        tc_commit(BAR(B_OREADY + w));
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_bf16_ts(tO, aP + uint32_t(8 * kk), dv + uint64_t(kk * (2048 >> 4)), idPV,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(BAR(B_OFULL + pb));
+                tc_commit(BAR(B_VEMPTY + s));
+                if (++s == NST) {
+                    s = 0;
+                    ph ^= 1u;
                 }
-                if (!ok) break;
-                tc_commit(BAR(B_KVEMPTY + s));
             }
             tc_commit(BAR(B_FINAL));
             for (int spin = 0; spin < (1 << 24); ++spin)
                 if (mbar_try_wait(BAR(B_FINAL), 0)) break;
         }
     } else if (warp < 8) {
-        const int w = warp >> 2;
-        const int sub = warp & 3;
-        const int r = sub * 32 + lane;
-        const int qrow = q0 + w * BM + r;
+        // ------------------------------------------------ softmax (warps 0..7)
+        const int half = lane >> 4;           // keys half*64 .. half*64+63 of each tile
+        const int rbase = 32 * (warp & 3) + 16 * (warp >> 2);
+        const int r = rbase + (lane & 15);    // row inside the query tile
+        const int qrow = q0 + r;
         const bool row_valid = qrow < seg_e;
-        const uint32_t lane_off = uint32_t(sub * 32) << 16;
-        const uint32_t tS = tmem + lane_off + uint32_t(w * 128);
-        const uint32_t tO = tmem + lane_off + uint32_t(256 + w * 128);
+        const uint32_t lane_off = uint32_t(rbase) << 16;
+        const uint32_t tO = tmem + lane_off + TM_O;
         const float c = p.sm_scale * 1.4426950408889634f;
+        const uint64_t c2 = f32x2_pack(c, c);
         float m_ref = 0.0f;
         float l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + w), j & 1, abort_flag, err));
+            const int sbuf = j & 1;
+            ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + sbuf), (j >> 1) & 1, abort_flag, err));
             if (!ok) break;
             tc_fence_after();
-            uint32_t s0[32], s1[32], s2[32], s3[32];
-            tmem_ld_32x32b_x32(tS + 0, s0);
-            tmem_ld_32x32b_x32(tS + 32, s1);
-            tmem_ld_32x32b_x32(tS + 64, s2);
-            tmem_ld_32x32b_x32(tS + 96, s3);
-            tmem_ld_wait(s0);
-            reg_fence32(s1);
-            reg_fence32(s2);
-            reg_fence32(s3);
-            float sf[128];
+            const uint32_t tS = tmem + lane_off + TM_S + uint32_t(sbuf * BN);
+            float s0[32], s1[32];
+            float m0, m1;
+            tmem_ld_16x2_x32_max<HALF>(tS + 0, s0, m0);
+            tmem_ld_16x2_x32_max<HALF>(tS + 32, s1, m1);
+            tmem_ld_wait_f32(s0);
+            reg_fence_f32(s1);
+            asm volatile("" : "+f"(m0), "+f"(m1));
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SFREE + sbuf));
+
+            float sf[HALF];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                sf[i] = __uint_as_float(s0[i]);
-                sf[32 + i] = __uint_as_float(s1[i]);
-                sf[64 + i] = __uint_as_float(s2[i]);
-                sf[96 + i] = __uint_as_float(s3[i]);
+                sf[i] = s0[i];
+                sf[32 + i] = s1[i];
             }
-            const int key0 = kbase + j * BN;
-            if (key0 + BN > seg_e) {
+            const int key0 = kbase + j * BN + half * HALF;
+            float pmax = fmaxf(m0, m1);
+            if (key0 + HALF > seg_e) {
+                // Last tile: keys past the segment are masked.
 #pragma unroll
-                for (int i = 0; i < 128; ++i)
+                for (int i = 0; i < HALF; ++i)
                     if (key0 + i >= seg_e) sf[i] = -INFINITY;
-            }
-            float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
+                float mx0 = sf[0], mx1 = sf[1];
 #pragma unroll
-            for (int i = 4; i < 128; i += 8) {
-                mx0 = fmax3(mx0, sf[i], sf[i + 1]);
-                mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
-                mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
-                mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
+                for (int i = 2; i + 4 <= HALF; i += 4) {
+                    mx0 = fmax3(mx0, sf[i], sf[i + 1]);
+                    mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
+                }
+                mx0 = fmax3(mx0, sf[HALF - 2], sf[HALF - 1]);
+                pmax = fmaxf(mx0, mx1);
             }
-            const float xmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+            pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, 16));
+            const float xmax = pmax * c;
             float oscale = 1.0f;
             bool need = false;
             if (j == 0) {
                 m_ref = ceilf(xmax);
-            } else if (xmax > m_ref) {
+            } else if (xmax > m_ref + RESCALE_AT) {
+                // bf16 and fp32 have range to spare: the reference moves only
+                // when P would pass 2^8.
                 const float mnew = ceilf(xmax);
                 oscale = exp2_int(m_ref - mnew);
                 l *= oscale;
                 m_ref = mnew;
                 need = true;
             }
-            const float bias = -m_ref;
-            // P (bf16) into the first 64 columns of S: keys 0..63 in columns
-            // 0..31, keys 64..127 in 32..63, two keys per column (lower key
-            // in the low half).  Each half is stored as soon as it is packed.
-            float ls = 0.f;
+            const uint64_t b2 = f32x2_pack(-m_ref, -m_ref);
+            // P = bf16(2^(x - m_ref)), two keys per 32-bit word (lower key in the
+            // low half); l adds the rounded weights (bf16 -> f32 is exact).
+            uint32_t pk[HALF / 2];
+            float la = 0.f, lb = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-                float la = 0.f, lb = 0.f;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float a0 = ex2_approx(fmaf(sf[64 * half + 2 * i], c, bias));
-                    const float a1 = ex2_approx(fmaf(sf[64 * half + 2 * i + 1], c, bias));
-                    pk[i] = cvt_bf16x2(a0, a1);
-                    // the row sum adds the weights as rounded (bf16 -> f32 is exact)
-                    const float r0 = __uint_as_float(pk[i] << 16);
-                    const float r1 = __uint_as_float(pk[i] & 0xFFFF0000u);
-                    if (i & 1) lb += r0 + r1; else la += r0 + r1;
-                }
-                ls += la + lb;
-                tmem_st_32x32b_x32(tS + uint32_t(32 * half), pk);
+            for (int q = 0; q < HALF / 2; ++q) {
+                float y0, y1;
+                f32x2_unpack(ffma2(f32x2_pack(sf[2 * q], sf[2 * q + 1]), c2, b2), y0, y1);
+                pk[q] = cvt_bf16x2(ex2_approx(y0), ex2_approx(y1));
+                const float r0 = __uint_as_float(pk[q] << 16);
+                const float r1 = __uint_as_float(pk[q] & 0xFFFF0000u);
+                if (q & 1) lb += r0 + r1; else la += r0 + r1;
             }
-            l += ls;
+            l += la + lb;
+
+            const int pb = j & 1;
             if (__any_sync(0xFFFFFFFFu, need)) {
-                for (int cc = 0; cc < p.DV; cc += 16) {
-                    uint32_t o[16];
-                    tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
-                    tmem_ld_wait16(o);
+                // O must hold every P.V before tile j: wait for P(j-1) V_{j-1}.
+                ok = __all_sync(0xFFFFFFFFu,
+                                bwait(BAR(B_OFULL + (pb ^ 1)), ((j - 1) >> 1) & 1, abort_flag, err));
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t s2v = f32x2_pack(oscale, oscale);
+                uint32_t oa[32], ob[32];
+                tmem_ld_16x2_x32<OSPLIT>(tO + 0u, oa);
+                tmem_ld_16x2_x32<OSPLIT>(tO + 32u, ob);
+                tmem_ld_wait(oa);
+                reg_fence32(ob);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * oscale);
-                    tmem_st_32x32b_x16(tO + uint32_t(cc), o);
+                for (int q = 0; q < 32; q += 2) {
+                    float a0, a1;
+                    f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(oa[q]), __uint_as_float(oa[q + 1])), s2v), a0, a1);
+                    oa[q] = __float_as_uint(a0);
+                    oa[q + 1] = __float_as_uint(a1);
+                    f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(ob[q]), __uint_as_float(ob[q + 1])), s2v), a0, a1);
+                    ob[q] = __float_as_uint(a0);
+                    ob[q + 1] = __float_as_uint(a1);
                 }
+                tmem_st_16x2_x32<OSPLIT>(tO + 0u, oa);
+                tmem_st_16x2_x32<OSPLIT>(tO + 32u, ob);
             }
+            if (j >= 2) {
+                // P buffer j % 2 is free once P(j-2) V_{j-2} is complete.
+                ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL + pb), ((j - 2) >> 1) & 1, abort_flag, err));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            // This half of the P row: 64 keys in 32 columns (lanes 16-31 at +32).
+            tmem_st_16x2_x32<HALF / 2>(tmem + lane_off + TM_P + uint32_t(pb * (BN / 2)), pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PFULL + w));
+            if (lane == 0) mbar_arrive(BAR(B_PFULL + pb));
         }
-        if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OREADY + w), 0, abort_flag, err));
+        if (ok)
+            ok = __all_sync(0xFFFFFFFFu,
+                            bwait(BAR(B_OFULL + ((nkv - 1) & 1)), ((nkv - 1) >> 1) & 1, abort_flag, err));
         if (ok) {
             tc_fence_after();
-            const float oscale = 1.0f / l;
+            const float oscale = 1.0f / (l + __shfl_xor_sync(0xFFFFFFFFu, l, 16));
             uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
-            for (int cc = 0; cc < p.DV; cc += 16) {
+            for (int cc = 0; cc < OSPLIT; cc += 16) {
                 uint32_t o[16];
-                tmem_ld_32x32b_x16(tO + uint32_t(cc), o);
+                tmem_ld_16x2_x16<OSPLIT>(tO + uint32_t(cc), o);
                 tmem_ld_wait16(o);
                 uint32_t pkd[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     pkd[q] = cvt_bf16x2(__uint_as_float(o[2 * q]) * oscale, __uint_as_float(o[2 * q + 1]) * oscale);
+                const int d0 = half * OSPLIT + cc;
                 if (row_valid) {
-                    if (cc + 8 <= p.D)
-                        *reinterpret_cast<uint4*>(orow + cc) = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
-                    if (cc + 16 <= p.D)
-                        *reinterpret_cast<uint4*>(orow + cc + 8) = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+                    if (d0 + 8 <= p.D)
+                        *reinterpret_cast<uint4*>(orow + d0) = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+                    if (d0 + 16 <= p.D)
+                        *reinterpret_cast<uint4*>(orow + d0 + 8) = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
                 }
             }
         }
