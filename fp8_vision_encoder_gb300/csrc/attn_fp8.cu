@@ -315,32 +315,16 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             // The loads also return each 32-key chunk's maximum (tcgen05.ld.red).
-            float s0[32], s1[32], s2[32], s3[32];
-            float m0, m1, m2, m3;
-            tmem_ld_16x2_x32_max<HALF>(tS + 0, s0, m0);
-            tmem_ld_16x2_x32_max<HALF>(tS + 32, s1, m1);
-            tmem_ld_16x2_x32_max<HALF>(tS + 64, s2, m2);
-            tmem_ld_16x2_x32_max<HALF>(tS + 96, s3, m3);
-            tmem_ld_wait_f32(s0);
-            reg_fence_f32(s1);
-            reg_fence_f32(s2);
-            reg_fence_f32(s3);
-            asm volatile("" : "+f"(m0), "+f"(m1), "+f"(m2), "+f"(m3));
+            float sf[128];
+            float mq[4];
+            tmem_ld_s128_max<HALF>(tS, sf, mq);
             // S(j) is in registers: the tensor core may overwrite it with S(j+1).
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SFREE));
 
-            float sf[128];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sf[i] = s0[i];
-                sf[32 + i] = s1[i];
-                sf[64 + i] = s2[i];
-                sf[96 + i] = s3[i];
-            }
             const int key0 = kbase + j * BN + half * HALF;
-            float pmax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            float pmax = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             if (key0 < seg_s || key0 + HALF > seg_e) {
                 // First or last tile: keys outside the segment are masked, and
                 // the maximum is taken over the keys left.
@@ -349,9 +333,12 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int key = key0 + i;
                     if (key < seg_s || key >= seg_e) sf[i] = -INFINITY;
                 }
-                float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
+                // Four running maxima over sf[0..127]: pairs 0..7 seed them,
+                // then eight values per step.
+                float mx0 = fmaxf(sf[0], sf[1]), mx1 = fmaxf(sf[2], sf[3]);
+                float mx2 = fmaxf(sf[4], sf[5]), mx3 = fmaxf(sf[6], sf[7]);
 #pragma unroll
-                for (int i = 4; i < 128; i += 8) {
+                for (int i = 8; i < 128; i += 8) {
                     mx0 = fmax3(mx0, sf[i], sf[i + 1]);
                     mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
                     mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
@@ -397,13 +384,8 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // scale columns 0..79, lanes 16-31 columns 80..159 (columns
                 // past DV + 16 are unused TMEM).
                 const uint64_t s2v = f32x2_pack(oscale, oscale);
-                uint32_t oa[32], ob[32], oc[16];
-                tmem_ld_16x2_x32<OSPLIT>(tO + 0u, oa);
-                tmem_ld_16x2_x32<OSPLIT>(tO + 32u, ob);
-                tmem_ld_16x2_x16<OSPLIT>(tO + 64u, oc);
-                tmem_ld_wait(oa);
-                reg_fence32(ob);
-                reg_fence16(oc);
+                uint32_t oa[32], ob[32], oc[16], lunused;
+                tmem_ld_o80<OSPLIT>(tO, tO + uint32_t(p.DV), oa, ob, oc, lunused);
 #pragma unroll
                 for (int q = 0; q < 32; q += 2) {
                     float a0, a1;
@@ -421,13 +403,10 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     oc[q] = __float_as_uint(a0);
                     oc[q + 1] = __float_as_uint(a1);
                 }
-                tmem_st_16x2_x32<OSPLIT>(tO + 0u, oa);
-                tmem_st_16x2_x32<OSPLIT>(tO + 32u, ob);
-                tmem_st_16x2_x16<OSPLIT>(tO + 64u, oc);
+                tmem_st_o80_sync<OSPLIT>(tO, oa, ob, oc);
             }
             // This half of the P row: 128 keys in 32 columns (lanes 16-31 at +32).
-            tmem_st_16x2_x32<HALF / 4>(tP, pk);
-            tmem_st_wait();
+            tmem_st_16x2_x32_sync<HALF / 4>(tP, pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_PFULL));
@@ -435,32 +414,29 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL), (nkv - 1) & 1, abort_flag, err));
         if (ok) {
             tc_fence_after();
-            uint32_t lbits;
-            tmem_ld_16x2_x1<1>(tO + uint32_t(p.DV), lbits);   // both halves: a copy of l
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            asm volatile("" : "+r"(lbits));
+            uint32_t lbits;   // both halves: a copy of l (column DV)
+            uint32_t oa[32], ob[32], oc[16];
+            tmem_ld_o80<OSPLIT>(tO, tO + uint32_t(p.DV), oa, ob, oc, lbits);
             const float oscale = p.st->scale[2] / __uint_as_float(lbits);
             uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
             const int cbase = half * OSPLIT;
-            for (int cc = 0; cc < OSPLIT; cc += 16) {
-                uint32_t o[16];
-                tmem_ld_16x2_x16<OSPLIT>(tO + uint32_t(cc), o);
-                tmem_ld_wait16(o);
-                uint32_t pkd[8];
+            auto store8 = [&](int d0, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                              uint32_t a5, uint32_t a6, uint32_t a7) {
+                if (!row_valid || d0 + 8 > p.D) return;
+                uint4 v;
+                v.x = cvt_bf16x2(__uint_as_float(a0) * oscale, __uint_as_float(a1) * oscale);
+                v.y = cvt_bf16x2(__uint_as_float(a2) * oscale, __uint_as_float(a3) * oscale);
+                v.z = cvt_bf16x2(__uint_as_float(a4) * oscale, __uint_as_float(a5) * oscale);
+                v.w = cvt_bf16x2(__uint_as_float(a6) * oscale, __uint_as_float(a7) * oscale);
+                *reinterpret_cast<uint4*>(orow + d0) = v;
+            };
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(o[2 * q]) * oscale,
-                                                              __uint_as_float(o[2 * q + 1]) * oscale);
-                    pkd[q] = *reinterpret_cast<uint32_t*>(&v2);
-                }
-                const int d0 = cbase + cc;
-                if (row_valid) {
-                    if (d0 + 8 <= p.D)
-                        *reinterpret_cast<uint4*>(orow + d0) = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
-                    if (d0 + 16 <= p.D)
-                        *reinterpret_cast<uint4*>(orow + d0 + 8) = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
-                }
+            for (int q = 0; q < 32; q += 8) {
+                store8(cbase + q, oa[q], oa[q + 1], oa[q + 2], oa[q + 3], oa[q + 4], oa[q + 5], oa[q + 6], oa[q + 7]);
+                store8(cbase + 32 + q, ob[q], ob[q + 1], ob[q + 2], ob[q + 3], ob[q + 4], ob[q + 5], ob[q + 6], ob[q + 7]);
             }
+            store8(cbase + 64, oc[0], oc[1], oc[2], oc[3], oc[4], oc[5], oc[6], oc[7]);
+            store8(cbase + 72, oc[8], oc[9], oc[10], oc[11], oc[12], oc[13], oc[14], oc[15]);
         }
     }
 

@@ -252,6 +252,76 @@ __device__ __forceinline__ void tmem_ld_16x2_x32_max(uint32_t taddr, float (&r)[
         : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31]), "=f"(mx)
         : "r"(taddr), "n"(SPLIT));
 }
+// Loads and their wait in ONE asm statement: the outputs of an asynchronous
+// tcgen05.ld exist only after tcgen05.wait::ld, and with separate statements
+// the compiler may copy or spill an output register in between (reading it too
+// early).  These helpers issue several loads, wait once, and only then define
+// their outputs.
+// 128 fp32 values per thread (four 32-column chunks at +0, +32, +64, +96, each
+// split by SPLIT columns between lanes 0-15 and 16-31) and each chunk's max.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld_s128_max(uint32_t taddr, float (&r)[128], float (&m)[4]) {
+    asm volatile(
+        "{\n\t.reg .b32 ta0, ta1, ta2, ta3;\n\t"
+        "mov.b32 ta0, %132;\n\t"
+        "add.u32 ta1, %132, 32;\n\t"
+        "add.u32 ta2, %132, 64;\n\t"
+        "add.u32 ta3, %132, 96;\n\t"
+        "tcgen05.ld.red.sync.aligned.16x32bx2.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %128, [ta0], %133;\n\t"
+        "tcgen05.ld.red.sync.aligned.16x32bx2.x32.max.f32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %129, [ta1], %133;\n\t"
+        "tcgen05.ld.red.sync.aligned.16x32bx2.x32.max.f32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, %130, [ta2], %133;\n\t"
+        "tcgen05.ld.red.sync.aligned.16x32bx2.x32.max.f32 {%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, %131, [ta3], %133;\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31]), "=f"(r[32]), "=f"(r[33]), "=f"(r[34]), "=f"(r[35]), "=f"(r[36]), "=f"(r[37]), "=f"(r[38]), "=f"(r[39]), "=f"(r[40]), "=f"(r[41]), "=f"(r[42]), "=f"(r[43]), "=f"(r[44]), "=f"(r[45]), "=f"(r[46]), "=f"(r[47]), "=f"(r[48]), "=f"(r[49]), "=f"(r[50]), "=f"(r[51]), "=f"(r[52]), "=f"(r[53]), "=f"(r[54]), "=f"(r[55]), "=f"(r[56]), "=f"(r[57]), "=f"(r[58]), "=f"(r[59]), "=f"(r[60]), "=f"(r[61]), "=f"(r[62]), "=f"(r[63]), "=f"(r[64]), "=f"(r[65]), "=f"(r[66]), "=f"(r[67]), "=f"(r[68]), "=f"(r[69]), "=f"(r[70]), "=f"(r[71]), "=f"(r[72]), "=f"(r[73]), "=f"(r[74]), "=f"(r[75]), "=f"(r[76]), "=f"(r[77]), "=f"(r[78]), "=f"(r[79]), "=f"(r[80]), "=f"(r[81]), "=f"(r[82]), "=f"(r[83]), "=f"(r[84]), "=f"(r[85]), "=f"(r[86]), "=f"(r[87]), "=f"(r[88]), "=f"(r[89]), "=f"(r[90]), "=f"(r[91]), "=f"(r[92]), "=f"(r[93]), "=f"(r[94]), "=f"(r[95]), "=f"(r[96]), "=f"(r[97]), "=f"(r[98]), "=f"(r[99]), "=f"(r[100]), "=f"(r[101]), "=f"(r[102]), "=f"(r[103]), "=f"(r[104]), "=f"(r[105]), "=f"(r[106]), "=f"(r[107]), "=f"(r[108]), "=f"(r[109]), "=f"(r[110]), "=f"(r[111]), "=f"(r[112]), "=f"(r[113]), "=f"(r[114]), "=f"(r[115]), "=f"(r[116]), "=f"(r[117]), "=f"(r[118]), "=f"(r[119]), "=f"(r[120]), "=f"(r[121]), "=f"(r[122]), "=f"(r[123]), "=f"(r[124]), "=f"(r[125]), "=f"(r[126]), "=f"(r[127]), "=f"(m[0]), "=f"(m[1]), "=f"(m[2]), "=f"(m[3])
+        : "r"(taddr), "n"(SPLIT)
+        : "memory");
+}
+// 80 columns per thread (32 at +0, 32 at +32, 16 at +64, split by SPLIT) and
+// one more word from `xaddr` (split 1), all loaded before one wait.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld_o80(uint32_t taddr, uint32_t xaddr, uint32_t (&oa)[32],
+                                            uint32_t (&ob)[32], uint32_t (&oc)[16], uint32_t& x) {
+    asm volatile(
+        "{\n\t.reg .b32 ta1, ta2;\n\t"
+        "add.u32 ta1, %81, 32;\n\t"
+        "add.u32 ta2, %81, 64;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%81], %83;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [ta1], %83;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79}, [ta2], %83;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x1.b32 {%80}, [%82], 1;\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
+        : "=r"(oa[0]), "=r"(oa[1]), "=r"(oa[2]), "=r"(oa[3]), "=r"(oa[4]), "=r"(oa[5]), "=r"(oa[6]), "=r"(oa[7]), "=r"(oa[8]), "=r"(oa[9]), "=r"(oa[10]), "=r"(oa[11]), "=r"(oa[12]), "=r"(oa[13]), "=r"(oa[14]), "=r"(oa[15]), "=r"(oa[16]), "=r"(oa[17]), "=r"(oa[18]), "=r"(oa[19]), "=r"(oa[20]), "=r"(oa[21]), "=r"(oa[22]), "=r"(oa[23]), "=r"(oa[24]), "=r"(oa[25]), "=r"(oa[26]), "=r"(oa[27]), "=r"(oa[28]), "=r"(oa[29]), "=r"(oa[30]), "=r"(oa[31]), "=r"(ob[0]), "=r"(ob[1]), "=r"(ob[2]), "=r"(ob[3]), "=r"(ob[4]), "=r"(ob[5]), "=r"(ob[6]), "=r"(ob[7]), "=r"(ob[8]), "=r"(ob[9]), "=r"(ob[10]), "=r"(ob[11]), "=r"(ob[12]), "=r"(ob[13]), "=r"(ob[14]), "=r"(ob[15]), "=r"(ob[16]), "=r"(ob[17]), "=r"(ob[18]), "=r"(ob[19]), "=r"(ob[20]), "=r"(ob[21]), "=r"(ob[22]), "=r"(ob[23]), "=r"(ob[24]), "=r"(ob[25]), "=r"(ob[26]), "=r"(ob[27]), "=r"(ob[28]), "=r"(ob[29]), "=r"(ob[30]), "=r"(ob[31]), "=r"(oc[0]), "=r"(oc[1]), "=r"(oc[2]), "=r"(oc[3]), "=r"(oc[4]), "=r"(oc[5]), "=r"(oc[6]), "=r"(oc[7]), "=r"(oc[8]), "=r"(oc[9]), "=r"(oc[10]), "=r"(oc[11]), "=r"(oc[12]), "=r"(oc[13]), "=r"(oc[14]), "=r"(oc[15]), "=r"(x)
+        : "r"(taddr), "r"(xaddr), "n"(SPLIT)
+        : "memory");
+}
+// A store and its wait in ONE asm statement: the source registers stay
+// untouched until tcgen05.wait::st has completed the store.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st_16x2_x32_sync(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%32], %33, {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        :
+        : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(taddr), "n"(SPLIT)
+        : "memory");
+}
+// O's 80 columns per thread (32 at +0, 32 at +32, 16 at +64, split by SPLIT)
+// stored back, then waited for, in one statement.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st_o80_sync(uint32_t taddr, const uint32_t (&oa)[32],
+                                                 const uint32_t (&ob)[32], const uint32_t (&oc)[16]) {
+    asm volatile(
+        "{\n\t.reg .b32 ta1, ta2;\n\t"
+        "add.u32 ta1, %80, 32;\n\t"
+        "add.u32 ta2, %80, 64;\n\t"
+        "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%80], %81, {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31};\n\t"
+        "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [ta1], %81, {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63};\n\t"
+        "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [ta2], %81, {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79};\n\t"
+        "tcgen05.wait::st.sync.aligned;\n\t}"
+        :
+        : "r"(oa[0]), "r"(oa[1]), "r"(oa[2]), "r"(oa[3]), "r"(oa[4]), "r"(oa[5]), "r"(oa[6]), "r"(oa[7]), "r"(oa[8]), "r"(oa[9]), "r"(oa[10]), "r"(oa[11]), "r"(oa[12]), "r"(oa[13]), "r"(oa[14]), "r"(oa[15]), "r"(oa[16]), "r"(oa[17]), "r"(oa[18]), "r"(oa[19]), "r"(oa[20]), "r"(oa[21]), "r"(oa[22]), "r"(oa[23]), "r"(oa[24]), "r"(oa[25]), "r"(oa[26]), "r"(oa[27]), "r"(oa[28]), "r"(oa[29]), "r"(oa[30]), "r"(oa[31]), "r"(ob[0]), "r"(ob[1]), "r"(ob[2]), "r"(ob[3]), "r"(ob[4]), "r"(ob[5]), "r"(ob[6]), "r"(ob[7]), "r"(ob[8]), "r"(ob[9]), "r"(ob[10]), "r"(ob[11]), "r"(ob[12]), "r"(ob[13]), "r"(ob[14]), "r"(ob[15]), "r"(ob[16]), "r"(ob[17]), "r"(ob[18]), "r"(ob[19]), "r"(ob[20]), "r"(ob[21]), "r"(ob[22]), "r"(ob[23]), "r"(ob[24]), "r"(ob[25]), "r"(ob[26]), "r"(ob[27]), "r"(ob[28]), "r"(ob[29]), "r"(ob[30]), "r"(ob[31]), "r"(oc[0]), "r"(oc[1]), "r"(oc[2]), "r"(oc[3]), "r"(oc[4]), "r"(oc[5]), "r"(oc[6]), "r"(oc[7]), "r"(oc[8]), "r"(oc[9]), "r"(oc[10]), "r"(oc[11]), "r"(oc[12]), "r"(oc[13]), "r"(oc[14]), "r"(oc[15]), "r"(taddr), "n"(SPLIT)
+        : "memory");
+}
 // Pins 32 fp32 registers after tcgen05.wait::ld (their loads are complete).
 __device__ __forceinline__ void tmem_ld_wait_f32(float (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" : "+f"(r[0]), "+f"(r[1]), "+f"(r[2]), "+f"(r[3]), "+f"(r[4]), "+f"(r[5]), "+f"(r[6]), "+f"(r[7]), "+f"(r[8]), "+f"(r[9]), "+f"(r[10]), "+f"(r[11]), "+f"(r[12]), "+f"(r[13]), "+f"(r[14]), "+f"(r[15]), "+f"(r[16]), "+f"(r[17]), "+f"(r[18]), "+f"(r[19]), "+f"(r[20]), "+f"(r[21]), "+f"(r[22]), "+f"(r[23]), "+f"(r[24]), "+f"(r[25]), "+f"(r[26]), "+f"(r[27]), "+f"(r[28]), "+f"(r[29]), "+f"(r[30]), "+f"(r[31]) : : "memory");
