@@ -286,6 +286,67 @@ def run_reference(args, ws, rank):
     return 0
 
 
+# Image sizes of the pages' encoder measurements ("FP8 ViT Encoder Attention",
+# Performance: HD, FullHD, QHD, 4K, 3 images per request) at 16-px patches.
+# 1080 px is not a multiple of 16: 67 patch rows are taken (the partial row
+# dropped), i.e. 67 x 120 = 8040 patches.
+SWEEP_SIZES = [("HD 720x1280", 45 * 80), ("FullHD 1080x1920", 67 * 120),
+               ("QHD 1440x2560", 90 * 160), ("4K 2160x3840", 135 * 240)]
+
+
+def resolution_sweep(vf, dev, stream, reps, head_dims=(80, 128), H=16, images=3):
+    """One attention layer per image size: FP8 with dynamic scaling (amax +
+    quant + attention), FP8 with static scales (quant + attention) and the BF16
+    path, each timed alone with CUDA events and L2 flushed before every rep;
+    prints one JSON line per (size, head_dim)."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for D in head_dims:
+        for name, L in SWEEP_SIZES:
+            seqlens = [L] * images
+            T = sum(seqlens)
+            cu = torch.tensor([i * L for i in range(images + 1)], dtype=torch.int32, device=dev)
+            q, k, v = workloads.make_qkv(seqlens, H, D, 900 + D, True, False, device=dev)
+            D_pad = vf.default_d_pad(D)
+            codes = vf.alloc_codes(T, H, D_pad, dev)
+            out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+            wsp = vf.Workspace(images, dev)
+            st_dyn = vf.ScaleState(dev).init()
+            st_sta = vf.ScaleState(dev).init().set_static(224.0, 198.0, 210.0)
+            attn = lambda st: vf.attn_varlen(*codes, st, cu, L, D, out=out, workspace=wsp, stream=stream)
+            quant = lambda st: vf.quantize_unpad(st, q, k, v, cu, D_pad=D_pad, out=codes, stream=stream)
+            arms = {
+                "fp8_dynamic": lambda: (vf.amax_update(st_dyn, q, k, v, cu, stream=stream),
+                                        quant(st_dyn), attn(st_dyn)),
+                "fp8_static": lambda: (quant(st_sta), attn(st_sta)),
+                "fp8_attn_only": lambda: attn(st_sta),
+                "bf16": lambda: vf.attn_varlen_bf16(q, k, v, cu, L, out=out, workspace=wsp,
+                                                    stream=stream),
+            }
+            res = {}
+            for arm, fn in arms.items():
+                for _ in range(3):
+                    fn()
+                times = []
+                for _ in range(reps):
+                    flush.fill_(1)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    torch.cuda.synchronize(dev)
+                    times.append(e0.elapsed_time(e1) * 1e3)
+                res[arm] = statistics.median(times)
+            assert wsp.error() == 0
+            flops = 4 * images * L * L * H * D
+            print(json.dumps({
+                "sweep": name, "tokens_per_image": L, "images": images, "heads": H, "head_dim": D,
+                **{k2 + "_us": round(v2, 1) for k2, v2 in res.items()},
+                "fp8_dynamic_vs_bf16": round(res["bf16"] / res["fp8_dynamic"], 3),
+                "fp8_static_vs_bf16": round(res["bf16"] / res["fp8_static"], 3),
+                "fp8_attn_tflops": round(flops / res["fp8_attn_only"] / 1e6, 1),
+                "bf16_tflops": round(flops / res["bf16"] / 1e6, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -298,6 +359,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison column")
     ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--sweep", action="store_true",
+               help="per image size: FP8 (dynamic / static, with quant) vs BF16 layer time, then exit")
+    ap.add_argument("--sweep-reps", type=int, default=7)
     args = ap.parse_args()
     ws, rank, local = _dist()
     if args.impl == "reference":
@@ -312,6 +376,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
+
+    if args.sweep:
+        resolution_sweep(vf, dev, torch.cuda.current_stream(dev), args.sweep_reps)
+        return 0
 
     w = workloads.WORKLOADS[args.workload]
     run = Runner(vf, w, dev, layers=args.layers)
