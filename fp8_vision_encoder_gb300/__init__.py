@@ -97,6 +97,10 @@ _state_init = _sig("vitfp8_scale_state_init", ctypes.c_int, [_vp, _vp])
 _set_static = _sig("vitfp8_set_static_scales", ctypes.c_int, [_vp, _f32, _f32, _f32, _vp])
 _amax_update = _sig("vitfp8_amax_update", ctypes.c_int,
                     [_vp, _vp, _vp, _vp, ctypes.POINTER(SrcLayout), _vp, _i32, _i32, _i32, _i32, _vp])
+_amax_local = _sig("vitfp8_amax_local", ctypes.c_int,
+                   [_vp, _vp, _vp, _vp, ctypes.POINTER(SrcLayout), _vp, _i32, _i32, _i32, _i32, _vp,
+                    _vp])
+_ring_push = _sig("vitfp8_ring_push", ctypes.c_int, [_vp, _vp, _vp])
 _quantize_unpad = _sig("vitfp8_quantize_unpad", ctypes.c_int,
                        [_vp, _vp, _vp, _vp, ctypes.POINTER(SrcLayout), _vp, _i32, _i32, _i32, _i32,
                         _i32, _vp, _vp, _vp, _vp])
@@ -203,6 +207,30 @@ def amax_update(state, q, k, v, cu_seqlens, total_tokens=None, layout=None, H=No
     lay = _layout_for(q, layout, H, D)
     _check(_amax_update(state.ptr, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(lay), _ptr(cu_seqlens),
                         nseq, int(T), int(H), int(D), _stream(stream)), "vitfp8_amax_update")
+
+
+def amax_local(state, q, k, v, cu_seqlens, total_tokens=None, layout=None, H=None, D=None,
+               out=None, stream=None):
+    """Data-parallel step 1: this rank's (amax_q, amax_k, amax_v, any_tokens) as a
+    float32[4] device tensor; the ring is not touched."""
+    nseq = _cu_info(cu_seqlens)
+    H = q.shape[-2] if H is None else H
+    D = q.shape[-1] if D is None else D
+    T = q.shape[0] if total_tokens is None else total_tokens
+    lay = _layout_for(q, layout, H, D)
+    if out is None:
+        out = torch.empty(4, dtype=torch.float32, device=q.device)
+    _check(_amax_local(state.ptr, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(lay), _ptr(cu_seqlens),
+                       nseq, int(T), int(H), int(D), _ptr(out), _stream(stream)),
+           "vitfp8_amax_local")
+    return out
+
+
+def ring_push(state, vals, stream=None):
+    """Data-parallel step 3: push reduced float32[4] values into the ring."""
+    if vals.dtype != torch.float32 or vals.numel() != 4 or not vals.is_cuda:
+        raise ValueError("vals must be a float32[4] CUDA tensor")
+    _check(_ring_push(state.ptr, _ptr(vals), _stream(stream)), "vitfp8_ring_push")
 
 
 def alloc_codes(T, H, D_pad, device="cuda"):

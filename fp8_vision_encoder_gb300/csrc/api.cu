@@ -59,7 +59,7 @@ const char* vitfp8_status_string(vitfp8_status s) {
     return "unknown status";
 }
 
-int32_t vitfp8_version(void) { return 100; }
+int32_t vitfp8_version(void) { return 101; }
 
 vitfp8_status vitfp8_scale_state_init(vitfp8_scale_state* d_state, cudaStream_t stream) {
     if (!d_state || !aligned4(d_state)) return VITFP8_ERR_INVALID_ARG;
@@ -86,10 +86,38 @@ vitfp8_status vitfp8_amax_update(vitfp8_scale_state* d_state, const vitfp8_bf16*
     s = check_src(h_layout, H, D, &L);
     if (s != VITFP8_OK) return s;
     if (num_seqs == 0 || total_tokens == 0) return VITFP8_OK;
-    return launch_amax(d_state, q, k, v, L, d_cu_seqlens, num_seqs, total_tokens, H, D, stream) ==
-                   cudaSuccess
+    return launch_amax(d_state, q, k, v, L, d_cu_seqlens, num_seqs, total_tokens, H, D, nullptr,
+                       stream) == cudaSuccess
                ? VITFP8_OK
                : VITFP8_ERR_CUDA;
+}
+
+vitfp8_status vitfp8_amax_local(vitfp8_scale_state* d_state, const vitfp8_bf16* q,
+                                const vitfp8_bf16* k, const vitfp8_bf16* v,
+                                const vitfp8_src_layout* h_layout, const int32_t* d_cu_seqlens,
+                                int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t D,
+                                float* d_vals, cudaStream_t stream) {
+    if (!d_vals || (reinterpret_cast<uintptr_t>(d_vals) & 3)) return VITFP8_ERR_INVALID_ARG;
+    vitfp8_status s = check_common(d_state, q, k, v, d_cu_seqlens, num_seqs, total_tokens, H, D);
+    if (s != VITFP8_OK) return s;
+    SrcDev L;
+    s = check_src(h_layout, H, D, &L);
+    if (s != VITFP8_OK) return s;
+    if (num_seqs == 0 || total_tokens == 0)
+        return cudaMemsetAsync(d_vals, 0, 4 * sizeof(float), stream) == cudaSuccess ? VITFP8_OK
+                                                                                    : VITFP8_ERR_CUDA;
+    return launch_amax(d_state, q, k, v, L, d_cu_seqlens, num_seqs, total_tokens, H, D, d_vals,
+                       stream) == cudaSuccess
+               ? VITFP8_OK
+               : VITFP8_ERR_CUDA;
+}
+
+vitfp8_status vitfp8_ring_push(vitfp8_scale_state* d_state, const float* d_vals,
+                               cudaStream_t stream) {
+    if (!d_state || !d_vals || (reinterpret_cast<uintptr_t>(d_state) & 3) ||
+        (reinterpret_cast<uintptr_t>(d_vals) & 3))
+        return VITFP8_ERR_INVALID_ARG;
+    return launch_ring_push(d_state, d_vals, stream) == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
 }
 
 int64_t vitfp8_vt_stride(int32_t total_tokens) {

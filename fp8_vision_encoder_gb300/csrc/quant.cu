@@ -104,11 +104,37 @@ __global__ void set_static_kernel(vitfp8_scale_state* st, float q, float k, floa
 
 // ---------------------------------------------------------------- amax
 
+// Push (a_q, a_k, a_v) into the ring, then recompute the reference and the
+// scales from the whole ring (push-then-scale).  One thread.
+__device__ void ring_push_scale(vitfp8_scale_state* st, const float (&a)[3]) {
+    const int pos = st->pos;
+    for (int t = 0; t < 3; ++t) {
+        st->amax_cur[t] = a[t];
+        st->hist[t][pos] = a[t];
+    }
+    st->pos = (pos + 1) % VITFP8_RING;
+    st->count = min(st->count + 1, VITFP8_RING);
+    for (int t = 0; t < 3; ++t) {
+        float A = 0.0f;
+        for (int i = 0; i < VITFP8_RING; ++i) A = fmaxf(A, st->hist[t][i]);
+        st->amax_ref[t] = A;
+        scale_from_amax(A, st->scale[t], st->inv_scale[t]);
+    }
+}
+
+// `out` null: the last block pushes the forward's amax into the ring.
+// `out` non-null (data-parallel step 1): the last block writes
+// (a_q, a_k, a_v, 1) there instead and leaves the ring alone; in static mode
+// block 0 writes zeros (nothing to reduce, nothing to push).
 __global__ void __launch_bounds__(QT_THREADS)
 amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
             const uint16_t* __restrict__ v, SrcDev L, const int32_t* __restrict__ cu, int nseq,
-            int T, int H, int D) {
-    if (st->mode != 0) return;  // static mode: nothing to track
+            int T, int H, int D, float* __restrict__ out) {
+    if (st->mode != 0) {  // static mode: nothing to track
+        if (out && threadIdx.x < 4 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+            out[threadIdx.x] = 0.0f;
+        return;
+    }
     const int z = blockIdx.z;
     const uint16_t* src = z == 0 ? q : (z == 1 ? k : v);
     const int t0 = blockIdx.x * QT_TOK;
@@ -159,24 +185,30 @@ amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16
     const unsigned prev = atomicAdd(&st->blocks_done, 1u);
     if (prev != total - 1) return;
 
-    // Last block: every other block's atomicMax is visible.  Push-then-scale.
+    // Last block: every other block's atomicMax is visible.
     __threadfence();
-    const int pos = st->pos;
+    float a[3];
     for (int t = 0; t < 3; ++t) {
         const uint32_t bits = atomicExch(&st->amax_bits[t], 0u);
-        const float a = __uint_as_float(bits << 16);
-        st->amax_cur[t] = a;
-        st->hist[t][pos] = a;
+        a[t] = __uint_as_float(bits << 16);
     }
-    st->pos = (pos + 1) % VITFP8_RING;
-    st->count = min(st->count + 1, VITFP8_RING);
-    for (int t = 0; t < 3; ++t) {
-        float A = 0.0f;
-        for (int i = 0; i < VITFP8_RING; ++i) A = fmaxf(A, st->hist[t][i]);
-        st->amax_ref[t] = A;
-        scale_from_amax(A, st->scale[t], st->inv_scale[t]);
+    if (out) {
+        for (int t = 0; t < 3; ++t) {
+            st->amax_cur[t] = a[t];
+            out[t] = a[t];
+        }
+        out[3] = 1.0f;
+    } else {
+        ring_push_scale(st, a);
     }
     st->blocks_done = 0u;
+}
+
+// Data-parallel step 3: push reduced values (a_q, a_k, a_v, any) if any > 0.
+__global__ void ring_push_kernel(vitfp8_scale_state* st, const float* __restrict__ vals) {
+    if (st->mode != 0 || !(vals[3] > 0.0f)) return;
+    const float a[3] = {vals[0], vals[1], vals[2]};
+    ring_push_scale(st, a);
 }
 
 // ---------------------------------------------------------------- quantize
@@ -283,9 +315,14 @@ cudaError_t launch_set_static(vitfp8_scale_state* st, float q, float k, float v,
 
 cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
                         const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
-                        int D, cudaStream_t s) {
+                        int D, float* out, cudaStream_t s) {
     dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
-    amax_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D);
+    amax_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ring_push(vitfp8_scale_state* st, const float* vals, cudaStream_t s) {
+    ring_push_kernel<<<1, 1, 0, s>>>(st, vals);
     return cudaGetLastError();
 }
 

@@ -149,6 +149,37 @@ vitfp8_status vitfp8_amax_update(vitfp8_scale_state* d_state, const vitfp8_bf16*
                                  cudaStream_t stream);
 
 /*
+ * Data-parallel dynamic scaling, step 1 of 3.  The amax of the pages is one
+ * value per tensor over the whole batch ("FP8 ViT Encoder Attention", Usage);
+ * when the batch's segments are spread over several GPUs, each rank computes
+ * the amax of its own tokens here, the ranks combine the four floats with an
+ * all-reduce(MAX) (step 2, the caller's collective), and every rank pushes
+ * the result with vitfp8_ring_push (step 3), so all rings stay identical to
+ * the single-GPU ring of the whole batch.  On one GPU,
+ * vitfp8_amax_local + vitfp8_ring_push == vitfp8_amax_update.
+ *
+ * Arguments as for vitfp8_amax_update, plus
+ *   d_vals: device float[4] (4-byte aligned), written on the stream with
+ *           (amax_q, amax_k, amax_v, 1) -- or (0, 0, 0, 0) when this rank has
+ *           no tokens (T == 0 or num_seqs == 0) or the state is static.
+ * The ring, pos, count and the scales are not changed; amax_cur gets the local amax.
+ */
+vitfp8_status vitfp8_amax_local(vitfp8_scale_state* d_state, const vitfp8_bf16* q,
+                                const vitfp8_bf16* k, const vitfp8_bf16* v,
+                                const vitfp8_src_layout* h_layout, const int32_t* d_cu_seqlens,
+                                int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t D,
+                                float* d_vals, cudaStream_t stream);
+
+/*
+ * Data-parallel dynamic scaling, step 3 of 3: push (d_vals[0..2]) into the
+ * ring and recompute amax_ref, scale and inv_scale exactly as
+ * vitfp8_amax_update does -- if d_vals[3] > 0 (some rank had tokens).
+ * No-op in static mode.  d_vals: device float[4], e.g. after all-reduce(MAX).
+ */
+vitfp8_status vitfp8_ring_push(vitfp8_scale_state* d_state, const float* d_vals,
+                               cudaStream_t stream);
+
+/*
  * Quantize + un-pad q, k and v in ONE launch ("FP8 ViT Encoder Attention",
  * intro and note: Q/K/V quantized on the fly before the attention call,
  * "quantization kernel launches + un-padding").
