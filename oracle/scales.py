@@ -60,25 +60,41 @@ class ScaleState:
         self.hist = np.zeros((3, RING), dtype=np.float32)
         self.pos = 0
         self.count = 0
-        self.mode = 0  # 0 dynamic, 1 static
+        self.mode = 0  # 0 dynamic (push, then scale), 1 static, 2 dynamic delayed
         self.amax_ref = np.zeros(3, dtype=np.float32)
         self.scale = np.ones(3, dtype=np.float32)
         self.inv_scale = np.ones(3, dtype=np.float32)
         self.amax_cur = np.zeros(3, dtype=np.float32)
 
+    def _scale_from_ring(self):
+        for t in range(3):
+            A = np.float32(self.hist[t].max())
+            self.amax_ref[t] = A
+            self.scale[t], self.inv_scale[t] = scale_pair(A)
+
     def push(self, amaxes):
-        """Dynamic mode, one forward: push amax of q, k, v, then rescale."""
-        if self.mode != 0:
+        """Dynamic mode, one forward.  Mode 0 follows the push-then-scale
+        reading: the forward's amax enters the ring, then the scale is taken
+        from the ring including it.  Mode 2 is delayed scaling: the scale is
+        taken from the ring as the earlier forwards left it, then the
+        forward's amax enters the ring.  Static mode ignores the call."""
+        if self.mode == 1:
             return
+        if self.mode == 2:
+            self._scale_from_ring()
         for t in range(3):
             self.amax_cur[t] = np.float32(amaxes[t])
             self.hist[t, self.pos] = np.float32(amaxes[t])
         self.pos = (self.pos + 1) % RING
         self.count = min(self.count + 1, RING)
-        for t in range(3):
-            A = np.float32(self.hist[t].max())
-            self.amax_ref[t] = A
-            self.scale[t], self.inv_scale[t] = scale_pair(A)
+        if self.mode == 0:
+            self._scale_from_ring()
+
+    def set_ring_order(self, delayed):
+        """Choose push-then-scale (False) or delayed scaling (True) for a
+        dynamic state; a static state is left as it is."""
+        if self.mode != 1:
+            self.mode = 2 if delayed else 0
 
     def set_static(self, q, k, v):
         """Static mode: the file's per-layer values become A for q, k, v."""

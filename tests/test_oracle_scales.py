@@ -105,3 +105,49 @@ def test_scale_file_aliases_and_roundtrip():
     out = calib.to_file_dict([(10.0, 20.0, 30.0)])
     assert out == {"visual.blocks.0.attn.attn": {"q": 15.0, "k": 30.0, "v": 45.0}}
     assert calib.DEFAULT_MARGIN == 1.5 and calib.CALIB_PASSES == 16
+
+
+def test_delayed_order_cold_start_uses_unit_scale():
+    # Delayed scaling: the first forward sees an empty ring (reading: empty
+    # slots hold 0, and a zero ring maximum gives scale = inv = 1).
+    st = scales.ScaleState()
+    st.set_ring_order(True)
+    st.push([100.0, 50.0, 25.0])
+    assert st.mode == 2
+    assert list(st.amax_ref) == [0.0, 0.0, 0.0]
+    assert list(st.scale) == [1.0, 1.0, 1.0] and list(st.inv_scale) == [1.0, 1.0, 1.0]
+    assert list(st.hist[:, 0]) == [100.0, 50.0, 25.0] and st.count == 1
+    st.push([1.0, 2.0, 3.0])
+    assert list(st.amax_ref) == [100.0, 50.0, 25.0]
+
+
+def test_delayed_order_against_previous_sixteen_bruteforce():
+    rng = np.random.default_rng(9)
+    st, now = scales.ScaleState(), scales.ScaleState()
+    st.set_ring_order(True)
+    seen = []
+    for n in range(40):
+        a = rng.uniform(0, 100, 3).astype(np.float32)
+        st.push(a)
+        now.push(a)
+        prev = seen[-16:]
+        for t in range(3):
+            want = max((x[t] for x in prev), default=np.float32(0.0))
+            assert st.amax_ref[t] == want
+            assert (st.scale[t], st.inv_scale[t]) == scales.scale_pair(want)
+        # the ring itself is the same as with push-then-scale
+        assert np.array_equal(st.hist, now.hist) and st.pos == now.pos and st.count == now.count
+        seen.append(a)
+
+
+def test_ring_order_leaves_static_alone():
+    st = scales.ScaleState()
+    st.set_static(224.0, 198.0, 210.0)
+    st.set_ring_order(True)
+    assert st.mode == 1
+    st.push([1.0, 1.0, 1.0])
+    assert list(st.amax_ref) == [224.0, 198.0, 210.0]
+    dyn = scales.ScaleState()
+    dyn.set_ring_order(True)
+    dyn.set_ring_order(False)
+    assert dyn.mode == 0
