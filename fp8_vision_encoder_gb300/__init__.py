@@ -97,6 +97,7 @@ _state_init = _sig("vitfp8_scale_state_init", ctypes.c_int, [_vp, _vp])
 _set_static = _sig("vitfp8_set_static_scales", ctypes.c_int, [_vp, _f32, _f32, _f32, _vp])
 _amax_update = _sig("vitfp8_amax_update", ctypes.c_int,
                     [_vp, _vp, _vp, _vp, ctypes.POINTER(SrcLayout), _vp, _i32, _i32, _i32, _i32, _vp])
+_set_ring_order = _sig("vitfp8_set_ring_order", ctypes.c_int, [_vp, _i32, _vp])
 _amax_local = _sig("vitfp8_amax_local", ctypes.c_int,
                    [_vp, _vp, _vp, _vp, ctypes.POINTER(SrcLayout), _vp, _i32, _i32, _i32, _i32, _vp,
                     _vp])
@@ -169,6 +170,12 @@ class ScaleState:
     def set_static(self, q, k, v, stream=None):
         _check(_set_static(self.ptr, float(q), float(k), float(v), _stream(stream)),
                "vitfp8_set_static_scales")
+        return self
+
+    def set_ring_order(self, delayed, stream=None):
+        """Dynamic mode: push-then-scale (delayed=False) or delayed scaling (True)."""
+        _check(_set_ring_order(self.ptr, 1 if delayed else 0, _stream(stream)),
+               "vitfp8_set_ring_order")
         return self
 
     def read(self):

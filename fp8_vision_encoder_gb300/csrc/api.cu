@@ -97,7 +97,7 @@ vitfp8_status vitfp8_amax_local(vitfp8_scale_state* d_state, const vitfp8_bf16* 
                                 const vitfp8_src_layout* h_layout, const int32_t* d_cu_seqlens,
                                 int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t D,
                                 float* d_vals, cudaStream_t stream) {
-    if (!d_vals || (reinterpret_cast<uintptr_t>(d_vals) & 3)) return VITFP8_ERR_INVALID_ARG;
+    if (!d_vals || !aligned4(d_vals)) return VITFP8_ERR_INVALID_ARG;
     vitfp8_status s = check_common(d_state, q, k, v, d_cu_seqlens, num_seqs, total_tokens, H, D);
     if (s != VITFP8_OK) return s;
     SrcDev L;
@@ -112,11 +112,16 @@ vitfp8_status vitfp8_amax_local(vitfp8_scale_state* d_state, const vitfp8_bf16* 
                : VITFP8_ERR_CUDA;
 }
 
+vitfp8_status vitfp8_set_ring_order(vitfp8_scale_state* d_state, int32_t delayed,
+                                    cudaStream_t stream) {
+    if (!d_state || !aligned4(d_state)) return VITFP8_ERR_INVALID_ARG;
+    return launch_set_ring_order(d_state, delayed ? 1 : 0, stream) == cudaSuccess ? VITFP8_OK
+                                                                                  : VITFP8_ERR_CUDA;
+}
+
 vitfp8_status vitfp8_ring_push(vitfp8_scale_state* d_state, const float* d_vals,
                                cudaStream_t stream) {
-    if (!d_state || !d_vals || (reinterpret_cast<uintptr_t>(d_state) & 3) ||
-        (reinterpret_cast<uintptr_t>(d_vals) & 3))
-        return VITFP8_ERR_INVALID_ARG;
+    if (!d_state || !d_vals || !aligned4(d_state) || !aligned4(d_vals)) return VITFP8_ERR_INVALID_ARG;
     return launch_ring_push(d_state, d_vals, stream) == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
 }
 

@@ -42,6 +42,7 @@ cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_
                         const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
                         int D, float* out, cudaStream_t s);
 cudaError_t launch_ring_push(vitfp8_scale_state* st, const float* vals, cudaStream_t s);
+cudaError_t launch_set_ring_order(vitfp8_scale_state* st, int delayed, cudaStream_t s);
 cudaError_t launch_quant(const vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
                          const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
                          int D, int Dp, uint8_t* q8, uint8_t* k8, uint8_t* v8t, int64_t Tv,

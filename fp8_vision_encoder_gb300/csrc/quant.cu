@@ -104,9 +104,22 @@ __global__ void set_static_kernel(vitfp8_scale_state* st, float q, float k, floa
 
 // ---------------------------------------------------------------- amax
 
-// Push (a_q, a_k, a_v) into the ring, then recompute the reference and the
-// scales from the whole ring (push-then-scale).  One thread.
+// Reference and scales from the ring maximum.  One thread.
+__device__ void scale_from_ring(vitfp8_scale_state* st) {
+    for (int t = 0; t < 3; ++t) {
+        float A = 0.0f;
+        for (int i = 0; i < VITFP8_RING; ++i) A = fmaxf(A, st->hist[t][i]);
+        st->amax_ref[t] = A;
+        scale_from_amax(A, st->scale[t], st->inv_scale[t]);
+    }
+}
+
+// One dynamic forward's ring update with (a_q, a_k, a_v).  Mode 0: push,
+// then scale from the ring including the push.  Mode 2 (delayed scaling):
+// scale from the ring the earlier forwards left, then push.  One thread.
 __device__ void ring_push_scale(vitfp8_scale_state* st, const float (&a)[3]) {
+    const bool delayed = st->mode == 2;
+    if (delayed) scale_from_ring(st);
     const int pos = st->pos;
     for (int t = 0; t < 3; ++t) {
         st->amax_cur[t] = a[t];
@@ -114,12 +127,11 @@ __device__ void ring_push_scale(vitfp8_scale_state* st, const float (&a)[3]) {
     }
     st->pos = (pos + 1) % VITFP8_RING;
     st->count = min(st->count + 1, VITFP8_RING);
-    for (int t = 0; t < 3; ++t) {
-        float A = 0.0f;
-        for (int i = 0; i < VITFP8_RING; ++i) A = fmaxf(A, st->hist[t][i]);
-        st->amax_ref[t] = A;
-        scale_from_amax(A, st->scale[t], st->inv_scale[t]);
-    }
+    if (!delayed) scale_from_ring(st);
+}
+
+__global__ void set_ring_order_kernel(vitfp8_scale_state* st, int delayed) {
+    if (st->mode != 1) st->mode = delayed ? 2 : 0;
 }
 
 // `out` null: the last block pushes the forward's amax into the ring.
@@ -130,7 +142,7 @@ __global__ void __launch_bounds__(QT_THREADS)
 amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
             const uint16_t* __restrict__ v, SrcDev L, const int32_t* __restrict__ cu, int nseq,
             int T, int H, int D, float* __restrict__ out) {
-    if (st->mode != 0) {  // static mode: nothing to track
+    if (st->mode == 1) {  // static mode: nothing to track
         if (out && threadIdx.x < 4 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
             out[threadIdx.x] = 0.0f;
         return;
@@ -206,7 +218,7 @@ amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16
 
 // Data-parallel step 3: push reduced values (a_q, a_k, a_v, any) if any > 0.
 __global__ void ring_push_kernel(vitfp8_scale_state* st, const float* __restrict__ vals) {
-    if (st->mode != 0 || !(vals[3] > 0.0f)) return;
+    if (st->mode == 1 || !(vals[3] > 0.0f)) return;
     const float a[3] = {vals[0], vals[1], vals[2]};
     ring_push_scale(st, a);
 }
@@ -318,6 +330,11 @@ cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_
                         int D, float* out, cudaStream_t s) {
     dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
     amax_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_ring_order(vitfp8_scale_state* st, int delayed, cudaStream_t s) {
+    set_ring_order_kernel<<<1, 1, 0, s>>>(st, delayed);
     return cudaGetLastError();
 }
 

@@ -76,7 +76,7 @@ typedef struct vitfp8_scale_state {
     float    hist[3][VITFP8_RING]; /* amax ring per tensor; empty slots hold 0 */
     int32_t  pos;                  /* slot the next forward writes */
     int32_t  count;                /* filled slots, <= 16 */
-    int32_t  mode;                 /* 0 dynamic, 1 static */
+    int32_t  mode;                 /* 0 dynamic, 1 static, 2 dynamic with delayed scaling */
     int32_t  dev_error;            /* first device-detected vitfp8_status, 0 if none */
     float    amax_ref[3];          /* A_t: ring maximum (dynamic) or the static value */
     float    scale[3];             /* A_t / 448 */
@@ -128,10 +128,25 @@ vitfp8_status vitfp8_set_static_scales(vitfp8_scale_state* d_state, float q, flo
                                        cudaStream_t stream);
 
 /*
+ * Order of the ring update in dynamic mode.  delayed = 0 (the default after
+ * init; mode 0): push the forward's amax, then take the scale from the ring
+ * including it, so the forward never saturates.  delayed != 0 (mode 2,
+ * delayed scaling): take the scale from the ring the earlier forwards left,
+ * then push -- the forward is quantized with its predecessors' history (the
+ * first forward with scale 1) and may saturate at +-448.  The pages describe
+ * the 16-entry ring ("FP8 ViT Encoder Attention", Usage) but not this order.
+ * A static state is left unchanged.  The ring contents are the same in both
+ * orders; only amax_ref / scale / inv_scale lag by one forward.
+ */
+vitfp8_status vitfp8_set_ring_order(vitfp8_scale_state* d_state, int32_t delayed,
+                                    cudaStream_t stream);
+
+/*
  * Dynamic scaling, one forward ("FP8 ViT Encoder Attention", Usage; Sonar,
  * Enable FP8 attention): amax of q, k and v over the valid tokens (all heads,
  * d < D), pushed into the 16-entry ring (push-then-scale), then
- * amax_ref = max(ring), scale and inv_scale recomputed.  One launch covers
+ * amax_ref = max(ring), scale and inv_scale recomputed (in mode 2 the
+ * scale is taken before the push; see vitfp8_set_ring_order).  One launch covers
  * all three tensors; the last block to finish updates the ring.
  * In static mode the launch returns without touching the state (a no-op).
  *

@@ -197,3 +197,34 @@ def test_full_size_codes_sampled_and_amax_exact(vf, name):
         got = codes[rows] if codes is not None else vthd[:, :, rows].permute(2, 0, 1)
         ref = oquant.quantize(np32(xs), ost.inv_scale[t])
         assert np.array_equal(got.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_delayed_ring_order(vf, split):
+    # Delayed scaling (mode 2): each forward is quantized with the scale of the
+    # ring its predecessors left; state and codes bit-exact with the oracle,
+    # through amax_update or through amax_local + ring_push.
+    seqlens, H, D = [333, 64, 200], 4, 80
+    cu, _ = cu_tensor(seqlens)
+    T = sum(seqlens)
+    st = vf.ScaleState().init().set_ring_order(True)
+    ost = oscales.ScaleState()
+    ost.set_ring_order(True)
+    for seed in range(20):
+        q, k, v = qkv(seqlens, H, D, 500 + seed, outliers=(seed % 3 == 0), per_head_std=True)
+        if split:
+            vf.ring_push(st, vf.amax_local(st, q, k, v, cu))
+        else:
+            vf.amax_update(st, q, k, v, cu)
+        oracle_push(ost, q, k, v)
+        state_matches(st.read(), ost)
+        q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
+        torch.cuda.synchronize()
+        for t, (codes, x) in enumerate(((q8, q), (k8, k), (vt_to_thd(v8t, T), v))):
+            check_codes(codes, x, ost.inv_scale[t], D, vf.default_d_pad(D))
+    assert st.read()["mode"] == 2 and st.device_error() == 0
+    # switching back, and a static state ignoring the order
+    st.set_ring_order(False)
+    assert st.read()["mode"] == 0
+    s2 = vf.ScaleState().init().set_static(224.0, 198.0, 210.0).set_ring_order(True)
+    assert s2.read()["mode"] == 1
