@@ -134,6 +134,46 @@ __global__ void set_ring_order_kernel(vitfp8_scale_state* st, int delayed) {
     if (st->mode != 1) st->mode = delayed ? 2 : 0;
 }
 
+// Block maximum of m (two bf16 magnitudes per 32-bit lane), one atomicMax into
+// the tensor's reduction word, and the launch's last block (atomic counter;
+// no grid barrier, no spin) either pushes the forward's amax into the ring or,
+// with `out`, writes (a_q, a_k, a_v, 1) there.
+__device__ __forceinline__ void amax_block_finish(vitfp8_scale_state* st, int z, uint32_t m,
+                                                  float* out, uint32_t* wmax) {
+    m = max(m & 0xFFFFu, m >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+
+    uint32_t bm = 0;
+#pragma unroll
+    for (int w = 0; w < QT_THREADS / 32; ++w) bm = max(bm, wmax[w]);
+    if (bm) atomicMax(&st->amax_bits[z], bm);
+    __threadfence();
+    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned prev = atomicAdd(&st->blocks_done, 1u);
+    if (prev != total - 1) return;
+
+    // Last block: every other block's atomicMax is visible.
+    __threadfence();
+    float a[3];
+    for (int t = 0; t < 3; ++t) {
+        const uint32_t bits = atomicExch(&st->amax_bits[t], 0u);
+        a[t] = __uint_as_float(bits << 16);
+    }
+    if (out) {
+        for (int t = 0; t < 3; ++t) {
+            st->amax_cur[t] = a[t];
+            out[t] = a[t];
+        }
+        out[3] = 1.0f;
+    } else {
+        ring_push_scale(st, a);
+    }
+    st->blocks_done = 0u;
+}
+
 // `out` null: the last block pushes the forward's amax into the ring.
 // `out` non-null (data-parallel step 1): the last block writes
 // (a_q, a_k, a_v, 1) there instead and leaves the ring alone; in static mode
@@ -182,38 +222,60 @@ amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16
             m = absmax_bf16x2(m, w[u].w);
         }
     }
-    m = max(m & 0xFFFFu, m >> 16);
-    m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x != 0) return;
+    amax_block_finish(st, z, m, out, wmax);
+}
 
-    uint32_t bm = 0;
-#pragma unroll
-    for (int w = 0; w < QT_THREADS / 32; ++w) bm = max(bm, wmax[w]);
-    if (bm) atomicMax(&st->amax_bits[z], bm);
-    __threadfence();
-    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
-    const unsigned prev = atomicAdd(&st->blocks_done, 1u);
-    if (prev != total - 1) return;
-
-    // Last block: every other block's atomicMax is visible.
-    __threadfence();
-    float a[3];
-    for (int t = 0; t < 3; ++t) {
-        const uint32_t bits = atomicExch(&st->amax_bits[t], 0u);
-        a[t] = __uint_as_float(bits << 16);
+// Same reduction when each token's heads are contiguous (head stride == D,
+// e.g. packed [T, H, D] or a fused QKV view): the amax is one value per
+// tensor, so a block reads whole token rows of H * D elements (long
+// coalesced runs) instead of one head's D-element slice per token.  Grid
+// (blocks, 1, 3); each block walks 16-token tiles, each warp two tokens of a
+// tile, 32 lanes x 16 bytes per step.
+constexpr int AR_TOK = 16;
+__global__ void __launch_bounds__(QT_THREADS)
+amax_rows_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q,
+                 const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, SrcDev L,
+                 const int32_t* __restrict__ cu, int nseq, int T, int H, int D,
+                 float* __restrict__ out) {
+    if (st->mode == 1) {
+        if (out && threadIdx.x < 4 && blockIdx.x == 0 && blockIdx.z == 0) out[threadIdx.x] = 0.0f;
+        return;
     }
-    if (out) {
-        for (int t = 0; t < 3; ++t) {
-            st->amax_cur[t] = a[t];
-            out[t] = a[t];
+    const int z = blockIdx.z;
+    const uint16_t* src = z == 0 ? q : (z == 1 ? k : v);
+    __shared__ int64_t rows[AR_TOK];
+    __shared__ uint32_t wmax[QT_THREADS / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int RV = H * (D >> 3);   // 16-byte vectors per token row
+    const int ntiles = (T + AR_TOK - 1) / AR_TOK;
+    uint32_t m = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        __syncthreads();   // the previous tile's rows[] are no longer read
+        if (threadIdx.x < AR_TOK) {
+            const int t = tile * AR_TOK + threadIdx.x;
+            rows[threadIdx.x] = t < T ? src_row_of(L, cu, nseq, t, &st->dev_error) : -1;
         }
-        out[3] = 1.0f;
-    } else {
-        ring_push_scale(st, a);
+        __syncthreads();
+        for (int tt = warp; tt < AR_TOK; tt += QT_THREADS / 32) {
+            const int64_t row = rows[tt];
+            if (row < 0) continue;
+            const uint16_t* p = src + row * L.ts;
+            for (int j = lane; j < RV; j += 4 * 32) {
+                uint4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    w[u] = j + 32 * u < RV ? ld_stream16(p + (j + 32 * u) * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    m = absmax_bf16x2(m, w[u].x);
+                    m = absmax_bf16x2(m, w[u].y);
+                    m = absmax_bf16x2(m, w[u].z);
+                    m = absmax_bf16x2(m, w[u].w);
+                }
+            }
+        }
     }
-    st->blocks_done = 0u;
+    amax_block_finish(st, z, m, out, wmax);
 }
 
 // Data-parallel step 3: push reduced values (a_q, a_k, a_v, any) if any > 0.
@@ -328,8 +390,15 @@ cudaError_t launch_set_static(vitfp8_scale_state* st, float q, float k, float v,
 cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
                         const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
                         int D, float* out, cudaStream_t s) {
-    dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
-    amax_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, out);
+    if (L.hs == D) {
+        // about 8 resident blocks of 256 threads per SM, shared by the 3 tensors
+        const int ntiles = (T + AR_TOK - 1) / AR_TOK;
+        dim3 grid(ntiles < 400 ? ntiles : 400, 1, 3);
+        amax_rows_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, out);
+    } else {
+        dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
+        amax_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, out);
+    }
     return cudaGetLastError();
 }
 

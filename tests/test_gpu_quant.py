@@ -228,3 +228,36 @@ def test_delayed_ring_order(vf, split):
     assert st.read()["mode"] == 0
     s2 = vf.ScaleState().init().set_static(224.0, 198.0, 210.0).set_ring_order(True)
     assert s2.read()["mode"] == 1
+
+
+@pytest.mark.parametrize("padded", [False, True])
+def test_head_stride_wider_than_d(vf, padded):
+    """Heads not contiguous within a token (head stride 96 > D = 80, the gap
+    holding huge values that must never be read): the amax takes the per-head
+    path; padded sources add padding rows that must not be read either."""
+    seqlens = [70, 0, 130, 9]
+    H, D, HS = 3, 80, 96
+    T = sum(seqlens)
+    q, k, v = qkv(seqlens, H, D, seed=31, outliers=True)
+    cu, _ = cu_tensor(seqlens)
+    wide = []
+    for x in (q, k, v):
+        w = torch.full((T, H, HS), 3.0e4, dtype=torch.bfloat16, device="cuda")
+        w[:, :, :D] = x
+        wide.append(w)
+    if padded:
+        s_max = 140
+        wide = [workloads.to_padded(w, seqlens, s_max, fill=3.0e4) for w in wide]
+        lay = vf.SrcLayout(1, 0, s_max, H * HS, HS)
+    else:
+        lay = vf.SrcLayout.packed(H, D, token_stride=H * HS, head_stride=HS)
+    st = vf.ScaleState().init()
+    ost = oscales.ScaleState()
+    for rep in range(2):
+        vf.amax_update(st, *wide, cu, total_tokens=T, layout=lay, H=H, D=D)
+        oracle_push(ost, q, k, v)
+        state_matches(st.read(), ost)
+    q8, k8, v8t = vf.quantize_unpad(st, *wide, cu, total_tokens=T, layout=lay, H=H, D=D)
+    torch.cuda.synchronize()
+    check_codes(q8, q, ost.inv_scale[0], D, vf.default_d_pad(D))
+    check_codes(vt_to_thd(v8t, T), v, ost.inv_scale[2], D, vf.default_d_pad(D))
