@@ -51,13 +51,6 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
                    "+r"(r[30]), "+r"(r[31]));
 }
 
-__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
-}
-
 // 2^k for an integer-valued float k in [-126, 0].
 __device__ __forceinline__ float exp2_int(float k) {
     int e = int(k) + 127;

@@ -110,17 +110,6 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]^T, E4M3 x E4M3 -> F32: A is read from tensor
-// memory (row i in lane i, four 8-bit K elements per 32-bit column).
-__device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // Four K-steps (K = 4 x 32) of D (+)= A[smem] B[smem]^T in one block: the
 // descriptors of step k are a + 2k and b + 2k (32 bytes further along the
 // 128-byte swizzled rows).  `accumulate` applies to step 0; steps 1-3 always
@@ -206,29 +195,6 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
-// 32 lanes x 32 columns of 32-bit TMEM words -> 32 registers per thread
-// (thread i of the warp gets lane base+i, columns col..col+31).
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 // Wait for this thread's tcgen05.ld results; the "+r" operands pin every use of
 // the loaded registers after the wait.
 // 16 lanes x 2 column ranges: thread t (t < 16) reads lane base + t at columns
@@ -338,51 +304,12 @@ __device__ __forceinline__ void tmem_ld_16x2_x16(uint32_t taddr, uint32_t (&r)[1
         : "r"(taddr), "n"(SPLIT));
 }
 template <int SPLIT>
-__device__ __forceinline__ void tmem_ld_16x2_x8(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-        : "r"(taddr), "n"(SPLIT));
-}
-template <int SPLIT>
-__device__ __forceinline__ void tmem_ld_16x2_x1(uint32_t taddr, uint32_t& r0) {
-    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x1.b32 {%0}, [%1], %2;" : "=r"(r0) : "r"(taddr), "n"(SPLIT));
-}
-template <int SPLIT>
 __device__ __forceinline__ void tmem_st_16x2_x32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.16x32bx2.x32.b32 "
         "[%32], %33, {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31};"
         :
         : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(taddr), "n"(SPLIT)
-        : "memory");
-}
-template <int SPLIT>
-__device__ __forceinline__ void tmem_st_16x2_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x32bx2.x16.b32 "
-        "[%16], %17, {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15};"
-        :
-        : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(taddr), "n"(SPLIT)
-        : "memory");
-}
-template <int SPLIT>
-__device__ __forceinline__ void tmem_st_16x2_x8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x32bx2.x8.b32 "
-        "[%8], %9, {%0,%1,%2,%3,%4,%5,%6,%7};"
-        :
-        : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(taddr), "n"(SPLIT)
-        : "memory");
-}
-template <int SPLIT>
-__device__ __forceinline__ void tmem_st_16x2_x4(uint32_t taddr, const uint32_t (&r)[4]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x32bx2.x4.b32 "
-        "[%4], %5, {%0,%1,%2,%3};"
-        :
-        : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(taddr), "n"(SPLIT)
         : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
@@ -405,40 +332,8 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
         :
         : "memory");
 }
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Per-thread register budget of the executing warpgroup (all its warps must
-// execute the same instruction).
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- math
@@ -485,25 +380,6 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
-}
-// Two E4M3 codes (bits 0..7, 8..15) -> f16x2, exact (E4M3 is a subset of f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
-    uint32_t d;
-    const uint16_t h = static_cast<uint16_t>(v);
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(h));
-    return d;
-}
-__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
-    float lo, hi;
-    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(v));
-    return make_float2(lo, hi);
 }
 // Two float32 -> bf16x2, round to nearest even; `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
