@@ -63,6 +63,16 @@ def test_ragged_segments(vf, D, outliers):
     assert_attention_ok(stats, "ragged D=%d outliers=%s" % (D, outliers), outliers)
 
 
+@pytest.mark.parametrize("D", [8, 16, 24, 40, 48, 56, 72, 88, 96, 104, 112, 120])
+def test_every_head_dim(vf, D):
+    """Every other supported head dim (multiples of 8 up to 128) on a ragged
+    batch with single-token segments and one segment spanning two key tiles."""
+    seqlens = [1, 130, 300, 9, 1]
+    r = _run(vf, seqlens, 2, D, [40 + D], outliers=False, per_head_std=True)
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], D)
+    assert_attention_ok(stats, "D=%d" % D)
+
+
 def test_d80_padded_codes(vf):
     r = _run(vf, [200, 333], 2, 80, [5], D_pad=96, per_head_std=True, outliers=False)
     stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 80)

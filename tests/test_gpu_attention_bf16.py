@@ -74,6 +74,13 @@ def test_ragged_segments(vf, D, outliers):
     _check(vf, out, q, k, v, cul, tag="ragged D=%d outliers=%s" % (D, outliers))
 
 
+@pytest.mark.parametrize("D", [8, 16, 24, 40, 48, 56, 88, 96, 104, 112, 120])
+def test_every_head_dim(vf, D):
+    seqlens = [1, 130, 300, 9, 1]
+    out, q, k, v, cu, cul = _run(vf, seqlens, 2, D, 40 + D, outliers=False, per_head_std=True)
+    _check(vf, out, q, k, v, cul, tag="D=%d" % D)
+
+
 def test_single_token_segments_copy_v(vf):
     """A segment of one token attends only to itself: o = v exactly."""
     seqlens = [1] * 37
