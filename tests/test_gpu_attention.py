@@ -9,8 +9,8 @@ import torch
 import workloads
 from oracle import scales as oscales
 
-from gpu_util import (assert_attention_ok, compare_attention, cu_tensor, np32, oracle_push, qkv,
-                      sample_rows, vt_to_thd)
+from gpu_util import (assert_attention_ok, check_codes, compare_attention, cu_tensor, np32,
+                      oracle_push, qkv, sample_rows, vt_to_thd)
 
 pytestmark = pytest.mark.gpu
 
@@ -212,3 +212,41 @@ def test_full_size_sampled_rows(vf, name, outliers):
     # the literal the benchmark spec bound: unit-normal inputs on the long benchmark shapes
     literal = (not has_outliers) and name in ("micro8k", "qhd3")
     assert_attention_ok(stats, "%s outliers=%s" % (name, has_outliers), has_outliers, literal)
+
+
+def test_buffers_beyond_2_gib():
+    """272 segments of 4096 tokens x 16 heads x d = 128 (T = 1 114 112): each
+    code buffer holds 2.28e9 elements and each bf16 source twice that in
+    bytes, so the last segment's element offsets pass 2^31 (64-bit index
+    arithmetic in the quantization, the tensor maps and the output stores).  Codes of the first and last segments
+    are checked bit for bit and sampled rows of both against the oracle."""
+    import fp8_vision_encoder_gb300 as vf
+    H, D, L, B = 16, 128, 4096, 272
+    T = L * B
+    cu, _ = cu_tensor([L] * B)
+    st = vf.ScaleState().init().set_static(224.0, 198.0, 210.0)
+    ost = oscales.ScaleState()
+    ost.set_static(224.0, 198.0, 210.0)
+    g = torch.Generator(device="cuda").manual_seed(2024)
+    src = []
+    for _ in range(3):
+        x = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
+        for c in range(0, T, 1 << 16):       # draw in 64 Ki-token chunks (bounded scratch)
+            x[c:c + (1 << 16)] = torch.randn((1 << 16, H, D), device="cuda", generator=g).to(torch.bfloat16)
+        src.append(x)
+    q, k, v = src
+    q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
+    ws = vf.Workspace(B)
+    out = vf.attn_varlen(q8, k8, v8t, st, cu, L, D, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.error() == 0 and st.device_error() == 0
+    assert (T - L) * H * D > 2 ** 31
+    rng = np.random.default_rng(3)
+    for s in (0, B - 1):
+        a, b = s * L, (s + 1) * L
+        check_codes(q8[a:b], q[a:b], ost.inv_scale[0], D, D)
+        check_codes(vt_to_thd(v8t[:, :, a:b], L), v[a:b], ost.inv_scale[2], D, D)
+        rows = np.sort(rng.choice(L, 24, replace=False))
+        stats = compare_attention(out[a:b], q8[a:b], k8[a:b], vt_to_thd(v8t[:, :, a:b], L),
+                                  list(ost.scale), [0, L], D, rows)
+        assert_attention_ok(stats, "segment %d of %d" % (s, B), literal=True)

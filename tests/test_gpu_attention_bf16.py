@@ -164,3 +164,30 @@ def test_full_size_sampled_rows(vf, name, outliers):
     has_outliers = outliers and w.outliers
     literal = (not has_outliers) and name in ("micro8k", "qhd3")
     _check(vf, out, q, k, v, cul, rows, literal, "%s outliers=%s" % (name, has_outliers))
+
+
+def test_buffers_beyond_2_gib(vf):
+    """272 segments of 4096 tokens x 16 heads x d = 128: the last segment's
+    element offsets in the bf16 q/k/v/out buffers pass 2^31."""
+    H, D, L, B = 16, 128, 4096, 272
+    T = L * B
+    cu, _ = cu_tensor([L] * B)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    src = []
+    for _ in range(3):
+        x = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
+        for c in range(0, T, 1 << 16):
+            x[c:c + (1 << 16)] = torch.randn((1 << 16, H, D), device="cuda", generator=g).to(torch.bfloat16)
+        src.append(x)
+    q, k, v = src
+    ws = vf.Workspace(B)
+    out = vf.attn_varlen_bf16(q, k, v, cu, L, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.error() == 0
+    assert (T - L) * H * D > 2 ** 31
+    rng = np.random.default_rng(4)
+    for s in (0, B - 1):
+        a, b = s * L, (s + 1) * L
+        rows = np.sort(rng.choice(L, 24, replace=False))
+        _check(vf, out[a:b], q[a:b], k[a:b], v[a:b], [0, L], rows=rows, literal=True,
+               tag="segment %d of %d" % (s, B))
