@@ -209,7 +209,7 @@ def test_full_size_sampled_rows(vf, name, outliers):
     rows = sample_rows(cul, 48, seed=1)
     stats = compare_attention(out, q8, k8, vt_to_thd(v8t, w.T), list(ost.scale), cul, w.D, rows)
     has_outliers = outliers and w.outliers
-    # the literal the benchmark spec bound: unit-normal inputs on the long benchmark shapes
+    # the literal bound (max |error| <= 2e-2) holds for unit-normal inputs on the long shapes
     literal = (not has_outliers) and name in ("micro8k", "qhd3")
     assert_attention_ok(stats, "%s outliers=%s" % (name, has_outliers), has_outliers, literal)
 
