@@ -292,9 +292,50 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
              const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, SrcDev L,
              const int32_t* __restrict__ cu, int nseq, int T, int H, int D, int Dp,
              uint8_t* __restrict__ q8, uint8_t* __restrict__ k8, uint8_t* __restrict__ v8t,
-             int64_t Tv, int32_t* err) {
+             int64_t Tv, int32_t* err, int rows_tok) {
     const int z = blockIdx.z;
     const uint16_t* src = z == 0 ? q : (z == 1 ? k : v);
+    if (z < 2 && rows_tok > 0) {
+        // Q and K with contiguous heads and no d padding (head stride == D ==
+        // D_pad): source and code rows are flat runs of H * D elements, so
+        // this block converts whole token rows -- `rows_tok` tokens from the
+        // block's flat index -- instead of one head's slice.  The grid is
+        // the one V's per-head transpose needs; rows_tok = ceil(64 / H)
+        // makes the row blocks cover all T tokens within it.
+        const int64_t flat = int64_t(blockIdx.y) * gridDim.x + blockIdx.x;
+        const int64_t r0 = flat * rows_tok;
+        if (r0 >= T) return;
+        const int RV = H * (D >> 3);
+        const float inv = st->inv_scale[z];
+        uint8_t* dst0 = z == 0 ? q8 : k8;
+        for (int tt = 0; tt < rows_tok; tt += 4) {
+            int64_t srow[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t t = r0 + tt + u;
+                srow[u] = (tt + u < rows_tok && t < T) ? src_row_of(L, cu, nseq, int(t), err) : -1;
+            }
+            for (int j = threadIdx.x; j < RV; j += QT_THREADS) {
+                uint4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    w[u] = srow[u] >= 0 ? ld_stream16(src + srow[u] * L.ts + int64_t(j) * 8)
+                                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t t = r0 + tt + u;
+                    if (tt + u >= rows_tok || t >= T) continue;
+                    uint2 o = make_uint2(0u, 0u);
+                    if (srow[u] >= 0) {
+                        o.x = quant4(w[u].x, w[u].y, inv);
+                        o.y = quant4(w[u].z, w[u].w, inv);
+                    }
+                    *reinterpret_cast<uint2*>(dst0 + t * (int64_t(H) * Dp) + int64_t(j) * 8) = o;
+                }
+            }
+        }
+        return;
+    }
     const int t0 = blockIdx.x * QT_TOK;
     const int h = blockIdx.y;
     __shared__ int64_t rows[QT_TOK];
@@ -418,8 +459,9 @@ cudaError_t launch_quant(const vitfp8_scale_state* st, const uint16_t* q, const 
                          cudaStream_t s) {
     dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
     int32_t* err = const_cast<int32_t*>(&st->dev_error);
+    const int rows_tok = (L.hs == D && Dp == D) ? (QT_TOK + H - 1) / H : 0;
     quant_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, Dp, q8, k8, v8t, Tv,
-                                             err);
+                                             err, rows_tok);
     return cudaGetLastError();
 }
 
