@@ -587,6 +587,22 @@ def e2e(vf, run, stream, dev, steps, ws, pg):
 
     one_step()
     torch.cuda.synchronize(dev)
+
+    # The host link alone, for reading the number: one layer's inputs in and
+    # one output out, each direction timed by itself.
+    def link_gbs(copy, nbytes, s):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        with torch.cuda.stream(s):
+            copy()
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        return nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+    h2d_link = link_gbs(lambda: [d.copy_(h, non_blocking=True) for d, h in zip(dev_in[0], host_in[0])],
+                        h2d // run.layers, s_in)
+    d2h_link = link_gbs(lambda: host_out[0].copy_(dev_out[0], non_blocking=True), d2h // run.layers,
+                        s_out)
     if pg:
         pg.barrier()
     a = torch.cuda.Event(enable_timing=True)
@@ -604,6 +620,8 @@ def e2e(vf, run, stream, dev, steps, ws, pg):
     val = ws * run.flops_layer * run.layers * steps / (ms * 1e-3) / 1e12
     return {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "link_gbs": {"h2d": h2d_link, "d2h": d2h_link,
+                         "step_floor_ms": h2d / (h2d_link * 1e6)},
             "copies": "pinned host buffers; H2D, compute and D2H on three streams, overlapped across layers"}
 
 
