@@ -116,6 +116,7 @@ _attn_bf16 = _sig("vitfp8_attn_varlen_bf16", ctypes.c_int,
                   [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, ctypes.c_size_t,
                    _vp])
 NOALLOC_MAX_SEQS = 4096
+_selftest_wait = _sig("vitfp8_selftest_bounded_wait", ctypes.c_int, [_vp, ctypes.c_size_t, _vp])
 _get_err = _sig("vitfp8_get_device_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 _get_ws_err = _sig("vitfp8_get_workspace_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 
@@ -279,6 +280,13 @@ class Workspace:
         _check(_get_ws_err(_ptr(self.buf), ctypes.byref(out), _stream(stream)),
                "vitfp8_get_workspace_error")
         return out.value
+
+
+def selftest_bounded_wait(workspace, stream=None):
+    """Run the kernels' bounded wait on a barrier nothing arrives on; afterwards
+    workspace.error() reads VITFP8_ERR_DEVICE_TIMEOUT (the wait gave up)."""
+    _check(_selftest_wait(_ptr(workspace.buf), workspace.nbytes, _stream(stream)),
+           "vitfp8_selftest_bounded_wait")
 
 
 def attn_varlen(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, out=None,

@@ -212,6 +212,13 @@ vitfp8_status vitfp8_get_device_error(const vitfp8_scale_state* d_state, int32_t
     return VITFP8_OK;
 }
 
+vitfp8_status vitfp8_selftest_bounded_wait(void* d_workspace, size_t workspace_bytes,
+                                          cudaStream_t stream) {
+    if (!d_workspace || workspace_bytes < sizeof(WsHeader) || !aligned4(d_workspace))
+        return VITFP8_ERR_INVALID_ARG;
+    return launch_selftest_wait(d_workspace, stream) == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
+}
+
 vitfp8_status vitfp8_get_workspace_error(const void* d_workspace, int32_t* h_out,
                                          cudaStream_t stream) {
     if (!d_workspace || !h_out) return VITFP8_ERR_INVALID_ARG;

@@ -49,6 +49,7 @@ cudaError_t launch_quant(const vitfp8_scale_state* st, const uint16_t* q, const 
                          cudaStream_t s);
 
 // ---- launchers (attn_fp8.cu)
+cudaError_t launch_selftest_wait(void* ws, cudaStream_t s);
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
                              void* ws, cudaStream_t s);
 vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,

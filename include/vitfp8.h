@@ -324,6 +324,18 @@ vitfp8_status vitfp8_get_device_error(const vitfp8_scale_state* d_state, int32_t
 vitfp8_status vitfp8_get_workspace_error(const void* d_workspace, int32_t* h_out,
                                          cudaStream_t stream);
 
+/*
+ * Failure-detection self-test: one warp runs the bounded mbarrier wait that
+ * every role of the attention kernels uses, on a barrier nothing arrives on.
+ * After the wait's limit (about 0.5 s) the kernel records
+ * VITFP8_ERR_DEVICE_TIMEOUT in the workspace error word (cleared at launch)
+ * and returns; read it with vitfp8_get_workspace_error.  Nothing traps,
+ * faults or hangs, and the context stays usable.
+ * d_workspace: at least vitfp8_attn_workspace_size(0) bytes, 4-byte aligned.
+ */
+vitfp8_status vitfp8_selftest_bounded_wait(void* d_workspace, size_t workspace_bytes,
+                                          cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

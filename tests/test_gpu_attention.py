@@ -250,3 +250,23 @@ def test_buffers_beyond_2_gib():
         stats = compare_attention(out[a:b], q8[a:b], k8[a:b], vt_to_thd(v8t[:, :, a:b], L),
                                   list(ost.scale), [0, L], D, rows)
         assert_attention_ok(stats, "segment %d of %d" % (s, B), literal=True)
+
+
+def test_bounded_wait_expires_into_a_status(vf):
+    """A wait on a barrier nothing arrives on gives up after its limit and
+    reports VITFP8_ERR_DEVICE_TIMEOUT through the workspace error word; the
+    context stays usable and the next call clears the word."""
+    import time
+    ws = vf.Workspace(1)
+    t0 = time.time()
+    vf.selftest_bounded_wait(ws)
+    assert ws.error() == 4          # VITFP8_ERR_DEVICE_TIMEOUT (this read synchronises)
+    assert 0.1 < time.time() - t0 < 30
+    r = _run(vf, [64, 192], 2, 128, [0], outliers=False)
+    assert r["ws"].error() == 0
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 128)
+    assert_attention_ok(stats, "after the timeout self-test")
+    # the same workspace, reused by an attention call, is cleared as well
+    cu, _ = cu_tensor([64, 192])
+    vf.attn_varlen(r["q8"], r["k8"], r["v8t"], r["st"], cu, 192, 128, workspace=ws)
+    assert ws.error() == 0
