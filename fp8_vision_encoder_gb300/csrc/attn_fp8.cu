@@ -450,24 +450,6 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
-// Self-test of the bounded wait every role of the attention kernels uses:
-// one warp waits on an mbarrier that nothing ever arrives on.  The wait must
-// give up after its limit (about half a second), record
-// VITFP8_ERR_DEVICE_TIMEOUT in the workspace error word and return, leaving
-// the context usable -- the failure is detected, not a hang or a fault.
-__global__ void selftest_wait_kernel(WsHeader* ws) {
-    __shared__ alignas(8) uint64_t bar;
-    __shared__ int abort_flag;
-    if (threadIdx.x == 0) {
-        ws->error = 0;
-        abort_flag = 0;
-        mbar_init(smem_u32(&bar), 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    bwait(smem_u32(&bar), 0, &abort_flag, &ws->error);
-}
-
 // Work list: segments sorted longest first (when there are at most 2048),
 // items per segment = ceil(L / rows_per_item) * H, prefix sums over the sorted order.
 __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T, int H,
@@ -555,11 +537,6 @@ cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows
     int32_t* order = reinterpret_cast<int32_t*>(hdr + 1);
     int32_t* prefix = order + nseq;
     attn_plan_kernel<<<1, 1024, 0, s>>>(cu, nseq, T, H, rows_per_item, hdr, order, prefix);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_selftest_wait(void* ws, cudaStream_t s) {
-    selftest_wait_kernel<<<1, 32, 0, s>>>(static_cast<WsHeader*>(ws));
     return cudaGetLastError();
 }
 
