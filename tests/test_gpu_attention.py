@@ -270,3 +270,14 @@ def test_bounded_wait_expires_into_a_status(vf):
     cu, _ = cu_tensor([64, 192])
     vf.attn_varlen(r["q8"], r["k8"], r["v8t"], r["st"], cu, 192, 128, workspace=ws)
     assert ws.error() == 0
+
+
+def test_more_segments_than_the_sorted_work_list():
+    """3000 segments of 0..24 tokens: past 2048 segments the work list keeps
+    the natural order instead of sorting longest first; every row checked."""
+    import fp8_vision_encoder_gb300 as vf
+    rng = np.random.default_rng(8)
+    seqlens = [int(x) for x in rng.integers(0, 25, 3000)]
+    r = _run(vf, seqlens, 3, 64, [9], outliers=False)
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 64)
+    assert_attention_ok(stats, "3000 segments")

@@ -191,3 +191,10 @@ def test_buffers_beyond_2_gib(vf):
         rows = np.sort(rng.choice(L, 24, replace=False))
         _check(vf, out[a:b], q[a:b], k[a:b], v[a:b], [0, L], rows=rows, literal=True,
                tag="segment %d of %d" % (s, B))
+
+
+def test_more_segments_than_the_sorted_work_list(vf):
+    rng = np.random.default_rng(8)
+    seqlens = [int(x) for x in rng.integers(0, 25, 3000)]
+    out, q, k, v, cu, cul = _run(vf, seqlens, 3, 64, 9, outliers=False)
+    _check(vf, out, q, k, v, cul, tag="3000 segments")
