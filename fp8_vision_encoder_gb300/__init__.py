@@ -148,9 +148,42 @@ def workspace_size(num_seqs):
     return int(_ws_size(int(num_seqs)))
 
 
+def _need_shape(t, dtype, shape, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must be a %s tensor of shape %s" % (name, dtype, tuple(shape)))
+
+
+def _need_placed(t, name):
+    if not t.is_contiguous() or not t.is_cuda:
+        raise ValueError("%s must be contiguous and on the GPU" % name)
+
+
+def _need(t, dtype, shape, name):
+    """Raise ValueError unless t is a contiguous CUDA tensor of this dtype and shape
+    (the library sees raw pointers and cannot check buffer sizes itself)."""
+    _need_shape(t, dtype, shape, name)
+    _need_placed(t, name)
+
+
+def _check_codes(q8, k8, v8t):
+    """q8, k8: uint8 [T, H, D_pad]; v8t: uint8 [H, D_pad, vt_stride(T)]."""
+    if not isinstance(q8, torch.Tensor) or q8.dim() != 3:
+        raise ValueError("q8 must be a uint8 tensor [T, H, D_pad]")
+    T, H, D_pad = q8.shape
+    want = ((q8, (T, H, D_pad), "q8"), (k8, (T, H, D_pad), "k8"), (v8t, (H, D_pad, vt_stride(T)), "v8t"))
+    for t, shape, name in want:
+        _need_shape(t, torch.uint8, shape, name)
+    for t, _, name in want:
+        _need_placed(t, name)
+    return T, H, D_pad
+
+
 def _cu_info(cu_seqlens):
-    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
-        raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+    if (not isinstance(cu_seqlens, torch.Tensor) or cu_seqlens.dtype != torch.int32
+            or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1):
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor [num_seqs + 1]")
+    if not cu_seqlens.is_contiguous() or not cu_seqlens.is_cuda:
+        raise ValueError("cu_seqlens must be contiguous and on the GPU")
     return cu_seqlens.numel() - 1
 
 
@@ -228,6 +261,7 @@ def amax_local(state, q, k, v, cu_seqlens, total_tokens=None, layout=None, H=Non
     lay = _layout_for(q, layout, H, D)
     if out is None:
         out = torch.empty(4, dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, (4,), "out")
     _check(_amax_local(state.ptr, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(lay), _ptr(cu_seqlens),
                        nseq, int(T), int(H), int(D), _ptr(out), _stream(stream)),
            "vitfp8_amax_local")
@@ -261,7 +295,13 @@ def quantize_unpad(state, q, k, v, cu_seqlens, total_tokens=None, D_pad=None, la
     T = q.shape[0] if total_tokens is None else total_tokens
     D_pad = default_d_pad(D) if D_pad is None else D_pad
     lay = _layout_for(q, layout, H, D)
-    q8, k8, v8t = alloc_codes(T, H, D_pad, q.device) if out is None else out
+    if out is None:
+        q8, k8, v8t = alloc_codes(T, H, D_pad, q.device)
+    else:
+        q8, k8, v8t = out
+        if tuple(q8.shape) != (T, H, D_pad):
+            raise ValueError("out[0] must have shape %s" % ((T, H, D_pad),))
+        _check_codes(q8, k8, v8t)
     _check(_quantize_unpad(state.ptr, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(lay),
                            _ptr(cu_seqlens), nseq, int(T), int(H), int(D), int(D_pad), _ptr(q8),
                            _ptr(k8), _ptr(v8t), _stream(stream)), "vitfp8_quantize_unpad")
@@ -293,11 +333,12 @@ def attn_varlen(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, ou
                 workspace=None, stream=None):
     """FP8 varlen attention -> bf16 [T, H, D]."""
     nseq = _cu_info(cu_seqlens)
-    T, H, D_pad = q8.shape
+    T, H, D_pad = _check_codes(q8, k8, v8t)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q8.device)
+    _need(out, torch.bfloat16, (T, H, D), "out")
     if workspace is None:
         workspace = Workspace(nseq, q8.device)
     _check(_attn(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq, int(max_seqlen),
@@ -318,6 +359,7 @@ def attn_varlen_bf16(q, k, v, cu_seqlens, max_seqlen, sm_scale=None, out=None, w
         sm_scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, (T, H, D), "out")
     if workspace is None:
         workspace = Workspace(nseq, q.device)
     _check(_attn_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseq, int(max_seqlen), int(T),
@@ -335,11 +377,12 @@ def attn_varlen_noalloc(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=
     ``out`` should be passed pre-allocated by such callers.
     """
     nseq = _cu_info(cu_seqlens)
-    T, H, D_pad = q8.shape
+    T, H, D_pad = _check_codes(q8, k8, v8t)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q8.device)
+    _need(out, torch.bfloat16, (T, H, D), "out")
     _check(_attn_noalloc(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq,
                          int(max_seqlen), int(T), int(H), int(D), int(D_pad), float(sm_scale),
                          _ptr(out), _stream(stream)), "vitfp8_attn_varlen_noalloc")
