@@ -589,15 +589,19 @@ def e2e(vf, run, stream, dev, steps, ws, pg):
     torch.cuda.synchronize(dev)
 
     # The host link alone, for reading the number: one layer's inputs in and
-    # one output out, each direction timed by itself.
+    # one output out, each direction timed by itself, best of three (the host
+    # side is shared, so a single copy can land in someone else's burst).
     def link_gbs(copy, nbytes, s):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        with torch.cuda.stream(s):
-            copy()
-        e1.record(s)
-        torch.cuda.synchronize(dev)
-        return nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        best = 0.0
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            with torch.cuda.stream(s):
+                copy()
+            e1.record(s)
+            torch.cuda.synchronize(dev)
+            best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        return best
 
     h2d_link = link_gbs(lambda: [d.copy_(h, non_blocking=True) for d, h in zip(dev_in[0], host_in[0])],
                         h2d // run.layers, s_in)
