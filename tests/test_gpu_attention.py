@@ -73,6 +73,22 @@ def test_every_head_dim(vf, D):
     assert_attention_ok(stats, "D=%d" % D)
 
 
+@pytest.mark.parametrize("factor", [0.25, 3.0])
+def test_softmax_scale_argument(vf, factor):
+    """sm_scale other than 1/sqrt(D) (a flatter and a sharper softmax; the
+    sharper one moves the row reference on more tiles)."""
+    D = 128
+    r = _run(vf, [300, 1000, 77], 2, D, [61], outliers=False)
+    sm_scale = factor / math.sqrt(D)
+    out = vf.attn_varlen(r["q8"], r["k8"], r["v8t"], r["st"], r["cu_t"], 1000, D, sm_scale=sm_scale,
+                         workspace=r["ws"])
+    torch.cuda.synchronize()
+    assert r["ws"].error() == 0
+    stats = compare_attention(out, r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], D,
+                              sm_scale=sm_scale)
+    assert_attention_ok(stats, "sm_scale x%.2f" % factor)
+
+
 def test_d80_padded_codes(vf):
     r = _run(vf, [200, 333], 2, 80, [5], D_pad=96, per_head_std=True, outliers=False)
     stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 80)

@@ -26,13 +26,15 @@ def vf():
     return vf
 
 
-def _check(vf, out, q, k, v, cul, rows=None, literal=False, tag=""):
+def _check(vf, out, q, k, v, cul, rows=None, literal=False, tag="", sm_scale=None):
     T, H, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
     qn, kn, vn = np32(q), np32(k), np32(v)
     if rows is None:
         rows = np.arange(T)
     rows = np.unique(np.asarray(rows, dtype=np.int64))
-    ref = oattn.attention_varlen(qn, kn, vn, cul, 1.0 / math.sqrt(D), rows)[rows]
+    ref = oattn.attention_varlen(qn, kn, vn, cul, sm_scale, rows)[rows]
     got = out[torch.from_numpy(rows).to(out.device)].float().cpu().numpy().astype(np.float64)
     err = got - ref
     v_max = float(np.abs(vn).max()) if vn.size else 0.0
@@ -72,6 +74,20 @@ def test_ragged_segments(vf, D, outliers):
     seqlens = [1, 127, 128, 129, 300, 17, 0, 5]
     out, q, k, v, cu, cul = _run(vf, seqlens, 3, D, 21, outliers)
     _check(vf, out, q, k, v, cul, tag="ragged D=%d outliers=%s" % (D, outliers))
+
+
+@pytest.mark.parametrize("factor", [0.25, 3.0])
+def test_softmax_scale_argument(vf, factor):
+    """sm_scale other than 1/sqrt(D): a flatter and a sharper softmax."""
+    seqlens, D = [300, 1000, 77], 128
+    cu, cul = cu_tensor(seqlens)
+    q, k, v = [t.cuda() for t in workloads.make_qkv(seqlens, 2, D, 61, False, False)]
+    sm_scale = factor / math.sqrt(D)
+    ws = vf.Workspace(len(seqlens))
+    out = vf.attn_varlen_bf16(q, k, v, cu, 1000, sm_scale=sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.error() == 0
+    _check(vf, out, q, k, v, cul, tag="sm_scale x%.2f" % factor, sm_scale=sm_scale)
 
 
 @pytest.mark.parametrize("D", [8, 16, 24, 40, 48, 56, 88, 96, 104, 112, 120])
