@@ -464,7 +464,7 @@ def main():
 
     # end to end through the public API with host buffers
     if not args.no_e2e:
-        line["e2e"] = e2e(vf, run, stream, dev, args.e2e_steps, ws, pg)
+        line["e2e"] = e2e(vf, run, stream, dev, args.e2e_steps, max(3, args.warmup), ws, pg)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, cores, desc, dt = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -520,7 +520,7 @@ def bf16_column(vf, run, stream, dev, steps, peaks, peak_kind, fp8_attn_us, fp8_
             "fp8_with_quant_speedup": attn_us / fp8_layer_us}
 
 
-def e2e(vf, run, stream, dev, steps, ws, pg):
+def e2e(vf, run, stream, dev, steps, warmup, ws, pg):
     """Same metric with pinned host inputs copied in and the output copied out every layer.
 
     The copies run on their own streams and overlap the compute of the
@@ -585,7 +585,11 @@ def e2e(vf, run, stream, dev, steps, ws, pg):
             out_free[b].record(s_out)
         stream.wait_stream(s_out)
 
-    one_step()
+    # Warm-up: the first pass over a freshly pinned host buffer is several
+    # times slower than later ones (256 ms against 69 ms for a 24-layer step),
+    # so the copies get the same warm-up steps as the compute.
+    for _ in range(warmup):
+        one_step()
     torch.cuda.synchronize(dev)
 
     # The host link alone, for reading the number: one layer's inputs in and
@@ -623,7 +627,7 @@ def e2e(vf, run, stream, dev, steps, ws, pg):
         ms = float(t.item())
     val = ws * run.flops_layer * run.layers * steps / (ms * 1e-3) / 1e12
     return {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "d2h_bytes_per_step": d2h, "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
             "link_gbs": {"h2d": h2d_link, "d2h": d2h_link,
                          "step_floor_ms": h2d / (h2d_link * 1e6)},
             "copies": "pinned host buffers; H2D, compute and D2H on three streams, overlapped across layers"}
