@@ -50,3 +50,44 @@ def test_reference_arm_two_ranks_prints_one_line():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_line(lines[0], 2)
+
+
+def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """SM clock median, max clock and throttle reasons from nvidia-smi's CSV
+    lines (a stand-in script on PATH prints three samples, then waits)."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text(
+        "#!/bin/sh\n"
+        "echo '0, 2070, 2070, 1201.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active'\n"
+        "echo '0, 1980, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active'\n"
+        "echo '0, 2070, 2070, 1100.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active'\n"
+        "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", str(tmp_path) + os.pathsep + os.environ["PATH"])
+    sys.path.insert(0, ROOT)
+    try:
+        import bench
+    finally:
+        sys.path.remove(ROOT)
+    import time
+    s = bench.ClockSampler(0)
+    s.start()
+    time.sleep(1.0)
+    r = s.stop()
+    assert r == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_records_the_timing_rules_reject():
+    sys.path.insert(0, ROOT)
+    try:
+        import bench
+    finally:
+        sys.path.remove(ROOT)
+    rec = lambda mhz, reasons: {"sm_mhz": mhz, "sm_max_mhz": 2070.0, "reasons": reasons, "samples": 9}
+    assert not bench.clocks_rejected(None)
+    assert not bench.clocks_rejected(rec(2070.0, []))
+    assert not bench.clocks_rejected(rec(1500.0, ["sw_power_cap"]))   # power cap: kept
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected(rec(2070.0, [r]))
+    assert bench.clocks_rejected(rec(1200.0, []))                      # held low, no reason
+    assert not bench.clocks_rejected(rec(1900.0, []))
