@@ -5,13 +5,14 @@ a rounding mode, a dropped saturation, swapped scale factors, a ring of the
 wrong length, the other ring order, a missing absolute value, a dropped
 softmax scale, a transposed score matrix, a wrong normaliser, keys taken
 across segments, a multiplier used as a divisor, a smaller P shift, a
-floored P reference -- by rewriting one line of its source (or one
+floored P reference, a scale file without its margin or with k and v
+swapped -- by rewriting one line of its source (or one
 constant), and checks that at least one pin below then fails.  The pins use
 only what the E4M3 format, the pages' values and library routines fix (the OCP
 value table, ties-to-even at every midpoint, saturation, torch's float8
 conversion, a deque of length 16, torch's float64 attention, segment
 independence, constant V, two worked P-requantization examples computed by
-hand from the E4M3 grid); none of them re-runs the oracle's own formula.
+hand from the E4M3 grid, the page's example scale file); none of them re-runs the oracle's own formula.
 With no mistake planted, every pin passes.
 """
 
@@ -26,9 +27,10 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import attention, e4m3, quant, scales
+from oracle import attention, calib, e4m3, quant, scales
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "e4m3_ocp_values.txt")
+SCALE_FILE = os.path.join(os.path.dirname(GOLDEN), "scale_file_example.json")
 
 
 # ---------------------------------------------------------------- pins
@@ -173,10 +175,26 @@ def pin_p8_far_keys_exact():
     assert abs(o[0, 0, 0] - exact) <= 1e-15 * exact
 
 
+def pin_scale_file_example():
+    # The page's example file: layer 0 holds q 224, k 198, v 210; layer 1
+    # q 218, k 195, v 207.  The same entry under the _scale aliases parses alike.
+    import json
+    d = json.load(open(SCALE_FILE))
+    assert calib.parse_file_dict(d) == {0: (224.0, 198.0, 210.0), 1: (218.0, 195.0, 207.0)}
+    alias = {"visual.blocks.3.attn.attn": {"q_scale": 1.0, "k_scale": 2.0, "v_scale": 3.0}}
+    assert calib.parse_file_dict(alias) == {3: (1.0, 2.0, 3.0)}
+
+
+def pin_margin():
+    # The 1.5 save margin on exactly representable values.
+    assert calib.saved_values([100.0, 200.0, 2.0]) == [150.0, 300.0, 3.0]
+    assert calib.layer_key(7) == "visual.blocks.7.attn.attn"
+
+
 PINS = [pin_decode_ocp_values, pin_encode_roundtrip_and_ties, pin_encode_saturation,
         pin_encode_torch, pin_scale_values, pin_amax, pin_ring_orders, pin_attention_sdpa,
         pin_attention_segments, pin_attention_constant_v, pin_quant_torch,
-        pin_p8_worked_example, pin_p8_far_keys_exact]
+        pin_p8_worked_example, pin_p8_far_keys_exact, pin_scale_file_example, pin_margin]
 
 
 # ---------------------------------------------------------------- mistakes
@@ -212,6 +230,10 @@ MUTANTS = {
     "P requantization: reference from floor": (attention, "_attend", [
         ("M = np.ceil(sc.max(axis=1, keepdims=True) / math.log(2.0))",
          "M = np.floor(sc.max(axis=1, keepdims=True) / math.log(2.0))")]),
+    "scale file: margin not applied": (calib, "saved_values", [
+        ("return [float(np.float32(x) * np.float32(margin)) for x in a]", "return [float(np.float32(x)) for x in a]")]),
+    "scale file: k and v entries swapped": (calib, "parse_file_dict", [
+        ('for t in ("q", "k", "v"):', 'for t in ("q", "v", "k"):')]),
     "quant: multiplier used as divisor": (quant, "quantize", [
         ("np.asarray(x, dtype=np.float32) * np.float32(inv)", "np.asarray(x, dtype=np.float32) / np.float32(inv)")]),
 }
