@@ -6,7 +6,7 @@ wrong length, the other ring order, a missing absolute value, a dropped
 softmax scale, a transposed score matrix, a wrong normaliser, keys taken
 across segments, a multiplier used as a divisor, a smaller P shift, a
 floored P reference, a scale file without its margin or with k and v
-swapped -- by rewriting one line of its source (or one
+swapped, padded rows or strides misplaced -- by rewriting one line of its source (or one
 constant), and checks that at least one pin below then fails.  The pins use
 only what the E4M3 format, the pages' values and library routines fix (the OCP
 value table, ties-to-even at every midpoint, saturation, torch's float8
@@ -191,10 +191,38 @@ def pin_margin():
     assert calib.layer_key(7) == "visual.blocks.7.attn.attn"
 
 
+def pin_unpad_layouts():
+    # A padded batch [B, s_max, H, D] with padding rows of huge values, and a
+    # fused [T, 3, H, D] QKV view, against packed rows cut out with numpy
+    # slicing: the same codes, padding never read.
+    rng = np.random.default_rng(7)
+    seqlens, H, D, s_max = [3, 5, 1], 2, 4, 6
+    cu = [0, 3, 8, 9]
+    packed = rng.standard_normal((9, H, D)).astype(np.float32)
+    padded = np.full((3, s_max, H, D), 3.0e4, np.float32)
+    for b, L in enumerate(seqlens):
+        padded[b, :L] = packed[cu[b]:cu[b + 1]]
+    inv = np.float32(10.0)
+    want = np.zeros((9, H, 8), np.uint8)
+    want[:, :, :D] = quant.quantize(packed, inv)
+    lay = quant.SrcLayout.padded_batch(s_max, H, D)
+    assert np.array_equal(quant.quantize_unpad(padded.ravel(), lay, cu, H, D, 8, inv), want)
+    fused = np.stack([packed * 0 + 7.0, packed, packed * 0 - 7.0], axis=1)   # k in the middle
+    lay_f = quant.SrcLayout(0, 0, 3 * H * D, D)
+    got = quant.quantize_unpad(fused.ravel()[H * D:], lay_f, cu, H, D, 8, inv)
+    assert np.array_equal(got, want)
+    # heads 6 elements apart, the 2 between them holding garbage
+    wide = np.full((9, H, 6), -3.0e4, np.float32)
+    wide[:, :, :D] = packed
+    lay_w = quant.SrcLayout(0, 0, H * 6, 6)
+    assert np.array_equal(quant.quantize_unpad(wide.ravel(), lay_w, cu, H, D, 8, inv), want)
+
+
 PINS = [pin_decode_ocp_values, pin_encode_roundtrip_and_ties, pin_encode_saturation,
         pin_encode_torch, pin_scale_values, pin_amax, pin_ring_orders, pin_attention_sdpa,
         pin_attention_segments, pin_attention_constant_v, pin_quant_torch,
-        pin_p8_worked_example, pin_p8_far_keys_exact, pin_scale_file_example, pin_margin]
+        pin_p8_worked_example, pin_p8_far_keys_exact, pin_scale_file_example, pin_margin,
+        pin_unpad_layouts]
 
 
 # ---------------------------------------------------------------- mistakes
@@ -234,6 +262,12 @@ MUTANTS = {
         ("return [float(np.float32(x) * np.float32(margin)) for x in a]", "return [float(np.float32(x)) for x in a]")]),
     "scale file: k and v entries swapped": (calib, "parse_file_dict", [
         ('for t in ("q", "k", "v"):', 'for t in ("q", "v", "k"):')]),
+    "un-padding: padded rows at b * (s_max - 1)": (quant, "source_rows", [
+        ("rows.append(b * layout.s_max + i)", "rows.append(b * (layout.s_max - 1) + i)")]),
+    "un-padding: head stride taken as D for every layout": (quant, "gather_valid", [
+        ("* layout.head_stride", "* D")]),
+    "un-padding: token stride taken as H * D": (quant, "gather_valid", [
+        ("idx = (rows[:, None, None] * layout.token_stride", "idx = (rows[:, None, None] * (H * D)")]),
     "quant: multiplier used as divisor": (quant, "quantize", [
         ("np.asarray(x, dtype=np.float32) * np.float32(inv)", "np.asarray(x, dtype=np.float32) / np.float32(inv)")]),
 }
