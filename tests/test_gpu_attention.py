@@ -89,6 +89,34 @@ def test_softmax_scale_argument(vf, factor):
     assert_attention_ok(stats, "sm_scale x%.2f" % factor)
 
 
+def test_saturating_static_scales(vf):
+    """Static values far below the data's magnitude (A = 0.5 for unit-normal
+    data with x20 outliers): most codes saturate to +-448; attention on those
+    codes still matches the oracle on the same codes."""
+    r = _run(vf, [300, 129], 2, 128, [71], static=(0.5, 0.5, 0.5), outliers=True)
+    q8 = r["q8"].cpu().numpy()
+    assert np.mean((q8 & 0x7F) == 0x7E) > 0.3
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 128)
+    assert_attention_ok(stats, "saturating static", outliers=True)
+
+
+def test_all_zero_inputs(vf):
+    """q = k = v = 0 in dynamic mode: amax 0, so scale = multiplier = 1, every
+    code 0x00, uniform attention over zeros: the output is exactly 0."""
+    seqlens, H, D = [200, 17], 2, 128
+    cu, _ = cu_tensor(seqlens)
+    z = torch.zeros((sum(seqlens), H, D), dtype=torch.bfloat16, device="cuda")
+    st = vf.ScaleState().init()
+    vf.amax_update(st, z, z, z, cu)
+    q8, k8, v8t = vf.quantize_unpad(st, z, z, z, cu)
+    out = vf.attn_varlen(q8, k8, v8t, st, cu, 200, D)
+    torch.cuda.synchronize()
+    s = st.read()
+    assert s["scale"] == [1.0, 1.0, 1.0] and s["inv_scale"] == [1.0, 1.0, 1.0] and s["count"] == 1
+    assert int(q8.count_nonzero()) == 0 and int(v8t.count_nonzero()) == 0
+    assert int(out.count_nonzero()) == 0 and st.device_error() == 0
+
+
 def test_d80_padded_codes(vf):
     r = _run(vf, [200, 333], 2, 80, [5], D_pad=96, per_head_std=True, outliers=False)
     stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 80)
