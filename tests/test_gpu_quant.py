@@ -103,6 +103,28 @@ def test_hd3_ring_wraps_d80(vf, D_pad):
     assert np.all(v8t[:, :, w.T:Tv].cpu().numpy() == 0)
 
 
+@pytest.mark.parametrize("D,D_pad", [(256, 256), (200, 256), (8, 16)])
+def test_largest_and_smallest_head_dims(vf, D, D_pad):
+    """Quantization takes head dims up to 256 (attention stops at 128): the
+    largest padded width, a ragged one below it, and the smallest."""
+    seqlens, H = [70, 1, 130], 3
+    T = sum(seqlens)
+    cu, _ = cu_tensor(seqlens)
+    q, k, v = qkv(seqlens, H, D, seed=17, per_head_std=True)
+    st = vf.ScaleState().init()
+    ost = oscales.ScaleState()
+    vf.amax_update(st, q, k, v, cu)
+    oracle_push(ost, q, k, v)
+    state_matches(st.read(), ost)
+    q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu, D_pad=D_pad)
+    torch.cuda.synchronize()
+    check_codes(q8, q, ost.inv_scale[0], D, D_pad)
+    check_codes(k8, k, ost.inv_scale[1], D, D_pad)
+    check_codes(vt_to_thd(v8t, T), v, ost.inv_scale[2], D, D_pad)
+    with pytest.raises(vf.VitFp8Error):
+        vf.quantize_unpad(st, q, k, v, cu, D_pad=D_pad + 16 if D_pad == 256 else 8)
+
+
 def test_ragged_tokens_and_zero_length_segment(vf):
     seqlens = [1, 127, 0, 129, 33, 200]
     H, D = 3, 64
