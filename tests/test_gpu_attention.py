@@ -89,6 +89,15 @@ def test_softmax_scale_argument(vf, factor):
     assert_attention_ok(stats, "sm_scale x%.2f" % factor)
 
 
+@pytest.mark.parametrize("H", [1, 40])
+def test_one_head_and_many_heads(vf, H):
+    """One head, and 40 heads (the whole-row quantization takes 2 tokens per
+    block then), on a ragged batch."""
+    r = _run(vf, [300, 65, 1], H, 64, [81], outliers=False, per_head_std=True)
+    stats = compare_attention(r["out"], r["q8"], r["k8"], r["v8"], r["scales"], r["cu"], 64)
+    assert_attention_ok(stats, "H=%d" % H)
+
+
 def test_saturating_static_scales(vf):
     """Static values far below the data's magnitude (A = 0.5 for unit-normal
     data with x20 outliers): most codes saturate to +-448; attention on those
