@@ -133,6 +133,9 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+L2_FLUSH_BYTES = 256 << 20   # twice the GB300's L2
+
+
 def clocks_rejected(clocks):
     """True for a clock record the timing rules reject: hw_slowdown,
     hw_thermal_slowdown or sw_thermal_slowdown active, or the median SM clock
@@ -312,7 +315,7 @@ def resolution_sweep(vf, dev, stream, reps, head_dims=(80, 128), H=16, images=3)
     quant + attention), FP8 with static scales (quant + attention) and the BF16
     path, each timed alone with CUDA events and L2 flushed before every rep;
     prints one JSON line per (size, head_dim)."""
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for D in head_dims:
         for name, L in SWEEP_SIZES:
             seqlens = [L] * images
@@ -402,10 +405,18 @@ def main():
         run.step(stream)
     torch.cuda.synchronize(dev)
 
+    # Every layer reads its own inputs.  A step whose inputs take at least
+    # twice the L2 leaves nothing in it for the next step; a smaller one gets
+    # the L2 flushed (a write of twice its size) before every timed step,
+    # outside the timed spans, which are then summed.
+    step_bytes = 3 * w.T * w.H * w.D * 2 * run.layers
+    flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+             if step_bytes < L2_FLUSH_BYTES else None)
+
     def timed_region():
         # Per-kernel events ride along on the timed steps.
-        start = torch.cuda.Event(enable_timing=True)
-        stop = torch.cuda.Event(enable_timing=True)
+        marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps if flush is not None else 1)]
         evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)]
                 for _ in range(run.layers)] for _ in range(args.steps)]
         sampler = ClockSampler(local)
@@ -414,15 +425,23 @@ def main():
         torch.cuda.synchronize(dev)
         sampler.start()
         time.sleep(0.3)
-        start.record(stream)
-        for s in range(args.steps):
-            run.step(stream, evs[s])
-        stop.record(stream)
+        if flush is None:
+            marks[0][0].record(stream)
+            for s in range(args.steps):
+                run.step(stream, evs[s])
+            marks[0][1].record(stream)
+        else:
+            for s in range(args.steps):
+                with torch.cuda.stream(stream):
+                    flush.fill_(s & 0xFF)
+                marks[s][0].record(stream)
+                run.step(stream, evs[s])
+                marks[s][1].record(stream)
         torch.cuda.synchronize(dev)
         clocks = sampler.stop()
         if pg:
             pg.barrier()
-        ms = start.elapsed_time(stop)
+        ms = sum(a.elapsed_time(b) for a, b in marks)
         if pg:
             t = torch.tensor([ms], device=dev)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -463,8 +482,11 @@ def main():
         "config": {"workload": w.desc, "name": w.name, "tokens": w.T, "segments": w.seqlens[:8],
                    "heads": w.H, "head_dim": w.D, "layers": run.layers,
                    "static_scales": run.static,
-                   "l2": "inputs larger than L2 (each layer reads its own %.0f MB of bf16 q/k/v)"
-                         % (3 * w.T * w.H * w.D * 2 / 1e6),
+                   "l2": (("inputs larger than L2 (each layer reads its own %.0f MB of bf16 q/k/v)"
+                           % (3 * w.T * w.H * w.D * 2 / 1e6)) if flush is None else
+                          ("L2 flushed (a %d MB write) before every timed step, outside the timed "
+                           "spans; a step reads %.0f MB of bf16 q/k/v" % (L2_FLUSH_BYTES >> 20,
+                                                                          step_bytes / 1e6))),
                    "parallelism": "replicas" if ws > 1 else "single"},
         "frac_of_fp8_peak": value / fp8_peak,
         "roofline": {"bound": "tensor", "kernel": "attn_fp8 (work-list + attention launch)",
