@@ -23,7 +23,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libvitfp8.so")
+# VITFP8_LIBRARY may name another build of the same library (the tests load
+# the bounds-checked build, libvitfp8_checked.so, this way in a subprocess).
+LIB_PATH = os.environ.get("VITFP8_LIBRARY") or os.path.join(_HERE, "libvitfp8.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -117,6 +119,8 @@ _attn_bf16 = _sig("vitfp8_attn_varlen_bf16", ctypes.c_int,
                    _vp])
 NOALLOC_MAX_SEQS = 4096
 _selftest_wait = _sig("vitfp8_selftest_bounded_wait", ctypes.c_int, [_vp, ctypes.c_size_t, _vp])
+_selftest_bounds = _sig("vitfp8_selftest_bounds_check", ctypes.c_int, [_vp, ctypes.c_size_t, _vp])
+_checked_build = _sig("vitfp8_checked_build", ctypes.c_int32, [])
 _get_err = _sig("vitfp8_get_device_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 _get_ws_err = _sig("vitfp8_get_workspace_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 
@@ -320,6 +324,18 @@ class Workspace:
         _check(_get_ws_err(_ptr(self.buf), ctypes.byref(out), _stream(stream)),
                "vitfp8_get_workspace_error")
         return out.value
+
+
+def checked_build():
+    """True when the loaded library is the bounds-checked build."""
+    return bool(_checked_build())
+
+
+def selftest_bounds_check(workspace, stream=None):
+    """Run the bounds-check self-test (records VITFP8_ERR_DEVICE_BOUNDS in the
+    workspace error word in the checked build, nothing in the normal one)."""
+    _check(_selftest_bounds(_ptr(workspace.buf), workspace.nbytes, _stream(stream)),
+           "vitfp8_selftest_bounds_check")
 
 
 def selftest_bounded_wait(workspace, stream=None):

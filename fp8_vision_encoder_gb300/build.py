@@ -17,6 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvitfp8.so")
+LIB_CHECKED = os.path.join(PKG, "libvitfp8_checked.so")
 SOURCES = ["api.cu", "quant.cu", "attn_fp8.cu", "attn_bf16.cu", "attn_noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -34,27 +35,34 @@ def _run(cmd):
     return r.stdout
 
 
-def build(verbose=False, extra_flags=()):
-    """Compile every CUDA source and link libvitfp8.so next to this file."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose=False, extra_flags=(), checked=False):
+    """Compile every CUDA source and link libvitfp8.so next to this file.
+
+    checked=True builds the bounds-checked variant (-DVITFP8_CHECKED) into
+    libvitfp8_checked.so instead, from its own object directory.
+    """
+    build_dir = BUILD + ("_checked" if checked else "")
+    lib = LIB_CHECKED if checked else LIB
+    flags = list(extra_flags) + (["-DVITFP8_CHECKED"] if checked else [])
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     objs = []
     cmds = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmds.append([nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj])
+        cmds.append([nvcc, *ARCH, *FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj])
     with ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         outs = list(ex.map(_run, cmds))
     if verbose:
         for o in outs:
             sys.stdout.write(o)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose="-v" in sys.argv, extra_flags=("-Xptxas", "-v") if "-v" in sys.argv else ())
-    print(LIB)
+    print(build(verbose="-v" in sys.argv, extra_flags=("-Xptxas", "-v") if "-v" in sys.argv else (),
+                checked="--checked" in sys.argv))

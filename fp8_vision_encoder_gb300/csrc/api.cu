@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "checked.cuh"
 #include "internal.cuh"
 #include "vitfp8.h"
 
@@ -25,7 +26,16 @@ vitfp8_status check_src(const vitfp8_src_layout* lay, int32_t H, int32_t D, SrcD
     out->s_max = lay->s_max;
     out->ts = lay->token_stride;
     out->hs = lay->head_stride;
+    out->extent = 0;
     return VITFP8_OK;
+}
+
+// Elements a source tensor holds under its layout: the last addressed row's
+// last head slice ends there (used by the checked build's bounds checks).
+int64_t src_extent(const SrcDev& L, int32_t num_seqs, int32_t T, int32_t H, int32_t D) {
+    const int64_t rows = L.padded ? int64_t(num_seqs) * L.s_max : int64_t(T);
+    if (rows <= 0) return 0;
+    return (rows - 1) * L.ts + int64_t(H - 1) * L.hs + D;
 }
 
 vitfp8_status check_common(const vitfp8_scale_state* st, const void* q, const void* k,
@@ -85,6 +95,7 @@ vitfp8_status vitfp8_amax_update(vitfp8_scale_state* d_state, const vitfp8_bf16*
     SrcDev L;
     s = check_src(h_layout, H, D, &L);
     if (s != VITFP8_OK) return s;
+    L.extent = src_extent(L, num_seqs, total_tokens, H, D);
     if (num_seqs == 0 || total_tokens == 0) return VITFP8_OK;
     return launch_amax(d_state, q, k, v, L, d_cu_seqlens, num_seqs, total_tokens, H, D, nullptr,
                        stream) == cudaSuccess
@@ -103,6 +114,7 @@ vitfp8_status vitfp8_amax_local(vitfp8_scale_state* d_state, const vitfp8_bf16* 
     SrcDev L;
     s = check_src(h_layout, H, D, &L);
     if (s != VITFP8_OK) return s;
+    L.extent = src_extent(L, num_seqs, total_tokens, H, D);
     if (num_seqs == 0 || total_tokens == 0)
         return cudaMemsetAsync(d_vals, 0, 4 * sizeof(float), stream) == cudaSuccess ? VITFP8_OK
                                                                                     : VITFP8_ERR_CUDA;
@@ -141,6 +153,7 @@ vitfp8_status vitfp8_quantize_unpad(const vitfp8_scale_state* d_state, const vit
     SrcDev L;
     s = check_src(h_layout, H, D, &L);
     if (s != VITFP8_OK) return s;
+    L.extent = src_extent(L, num_seqs, total_tokens, H, D);
     if (D_pad < D || (D_pad & 15)) return VITFP8_ERR_INVALID_ARG;
     if (D_pad > 256) return VITFP8_ERR_UNSUPPORTED;
     if (num_seqs == 0 || total_tokens == 0) return VITFP8_OK;
@@ -218,6 +231,15 @@ vitfp8_status vitfp8_selftest_bounded_wait(void* d_workspace, size_t workspace_b
         return VITFP8_ERR_INVALID_ARG;
     return launch_selftest_wait(d_workspace, stream) == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
 }
+
+vitfp8_status vitfp8_selftest_bounds_check(void* d_workspace, size_t workspace_bytes,
+                                           cudaStream_t stream) {
+    if (!d_workspace || workspace_bytes < sizeof(WsHeader) || !aligned4(d_workspace))
+        return VITFP8_ERR_INVALID_ARG;
+    return launch_selftest_bounds(d_workspace, stream) == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
+}
+
+int32_t vitfp8_checked_build(void) { return VF_CHECKED_BUILD; }
 
 vitfp8_status vitfp8_get_workspace_error(const void* d_workspace, int32_t* h_out,
                                          cudaStream_t stream) {

@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
+#include "host_once.h"
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -83,9 +84,12 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     int lo = 0, hi = p.nseq - 1;  // largest pos with prefix[pos] <= item
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
+        if (!VF_IN(mid, 1, p.nseq + 1, &p.ws->error)) return;
         if (p.prefix[mid] <= item) lo = mid; else hi = mid - 1;
     }
+    if (!VF_IN(lo, 1, p.nseq, &p.ws->error)) return;
     const int b = p.order[lo];
+    if (!VF_IN(b, 2, p.nseq + 1, &p.ws->error)) return;
     const int local = item - p.prefix[lo];
     const int seg_s = p.cu[b];
     const int seg_e = p.cu[b + 1];
@@ -286,7 +290,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 // Last tile: keys past the segment are masked.
 #pragma unroll
                 for (int i = 0; i < HALF; ++i)
-                    if (key0 + i >= seg_e) sf[i] = -INFINITY;
+                    if (key0 + i >= seg_e && VF_IN(i, 1, HALF, err)) sf[i] = -INFINITY;
                 float mx0 = sf[0], mx1 = sf[1];
 #pragma unroll
                 for (int i = 2; i + 4 <= HALF; i += 4) {
@@ -383,9 +387,10 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     pkd[q] = cvt_bf16x2(__uint_as_float(o[2 * q]) * oscale, __uint_as_float(o[2 * q + 1]) * oscale);
                 const int d0 = half * OSPLIT + cc;
                 if (row_valid) {
-                    if (d0 + 8 <= p.D)
+                    const int64_t o0 = (int64_t(qrow) * p.H + h) * p.D + d0;
+                    if (d0 + 8 <= p.D && VF_IN(o0, 8, p.out_elems, err))
                         *reinterpret_cast<uint4*>(orow + d0) = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
-                    if (d0 + 16 <= p.D)
+                    if (d0 + 16 <= p.D && VF_IN(o0 + 8, 8, p.out_elems, err))
                         *reinterpret_cast<uint4*>(orow + d0 + 8) = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
                 }
             }
@@ -404,16 +409,18 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 namespace {
 using EncodeFnB = decltype(&cuTensorMapEncodeTiled);
 
+// cuTensorMapEncodeTiled from the driver, looked up once per process
+// (thread-safe static initialisation); null if unavailable.
 EncodeFnB get_encode_fn_b() {
-    static EncodeFnB fn = nullptr;
-    if (!fn) {
+    static const EncodeFnB fn = []() -> EncodeFnB {
         cudaDriverEntryPointQueryResult q;
         void* ptr = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFnB>(ptr);
-    }
+            return reinterpret_cast<EncodeFnB>(ptr);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -429,6 +436,9 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int T, int H, int D) {
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// Dynamic shared memory opt-in, once per device (a per-device attribute).
+PerDeviceOnce g_smem_attr_b;
 }  // namespace
 
 vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -440,13 +450,13 @@ vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint1
         !make_map_bf16(&mv, v, T, H, D))
         return VITFP8_ERR_CUDA;
     if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, ws, s) != cudaSuccess) return VITFP8_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return VITFP8_ERR_CUDA;
-        attr_set = true;
-    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VITFP8_ERR_CUDA;
+    if (!g_smem_attr_b.run(dev, [] {
+            return cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES) == cudaSuccess;
+        }))
+        return VITFP8_ERR_CUDA;
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     AttnParams prm;
     prm.cu = cu;
@@ -459,9 +469,11 @@ vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint1
     prm.T = T;
     prm.H = H;
     prm.D = D;
+    prm.Dp = D;
     prm.DV = (D + 15) & ~15;
     prm.KS = (D + 15) / 16;
     prm.sm_scale = sm_scale;
+    prm.out_elems = int64_t(T) * H * D;
     const long long grid = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H;
     if (grid > 0x7FFFFFFFLL) return VITFP8_ERR_UNSUPPORTED;
     attn_bf16_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 
+#include "checked.cuh"
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -18,8 +19,9 @@ struct AttnParams {
     WsHeader* ws;
     const vitfp8_scale_state* st;
     uint16_t* out;
-    int nseq, T, H, D, DV, KS;
+    int nseq, T, H, D, Dp, DV, KS;
     float sm_scale;
+    int64_t out_elems;  // T * H * D (checked build)
 };
 
 // Bounded wait: true when the phase with `parity` completed; false if the CTA

@@ -62,6 +62,7 @@
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
+#include "host_once.h"
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -122,9 +123,12 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     int lo = 0, hi = p.nseq - 1;  // largest pos with prefix[pos] <= item
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
+        if (!VF_IN(mid, 1, p.nseq + 1, &p.ws->error)) return;
         if (p.prefix[mid] <= item) lo = mid; else hi = mid - 1;
     }
+    if (!VF_IN(lo, 1, p.nseq, &p.ws->error)) return;
     const int b = p.order[lo];
+    if (!VF_IN(b, 2, p.nseq + 1, &p.ws->error)) return;
     const int local = item - p.prefix[lo];
     const int seg_s = p.cu[b];
     const int seg_e = p.cu[b + 1];
@@ -153,7 +157,8 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int i = threadIdx.x; i < NST * 2 * 16 * 32; i += blockDim.x) {
         const int blk = i / (16 * 32);
         const int w = i - blk * (16 * 32);
-        reinterpret_cast<uint32_t*>(smem + SM_V + blk * VBLK + p.DV * 128)[w] = 0x38383838u;
+        if (VF_IN(blk * VBLK + p.DV * 128 + 4 * w, 4, NST * VBYTES, &p.ws->error))
+            reinterpret_cast<uint32_t*>(smem + SM_V + blk * VBLK + p.DV * 128)[w] = 0x38383838u;
     }
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
@@ -194,6 +199,12 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (; j < nkv; ++j) {
                 const int s = j % NST;
                 const int key0 = kbase + j * BN;
+                if (VF_CHECKED_BUILD && (key0 & 15) != 0) {
+                    // V^T copies start at token key0: TMA needs it 16-byte aligned.
+                    record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
+                    *abort_flag = 1;
+                    break;
+                }
                 if (j >= NST && !bwait(BAR(B_KEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
                 mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
                 tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, key0);
@@ -331,7 +342,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int i = 0; i < 128; ++i) {
                     const int key = key0 + i;
-                    if (key < seg_s || key >= seg_e) sf[i] = -INFINITY;
+                    if ((key < seg_s || key >= seg_e) && VF_IN(i, 1, 128, err)) sf[i] = -INFINITY;
                 }
                 // Four running maxima over sf[0..127]: pairs 0..7 seed them,
                 // then eight values per step.
@@ -423,6 +434,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             auto store8 = [&](int d0, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
                               uint32_t a5, uint32_t a6, uint32_t a7) {
                 if (!row_valid || d0 + 8 > p.D) return;
+                if (!VF_IN((int64_t(qrow) * p.H + h) * p.D + d0, 8, p.out_elems, err)) return;
                 uint4 v;
                 v.x = cvt_bf16x2(__uint_as_float(a0) * oscale, __uint_as_float(a1) * oscale);
                 v.y = cvt_bf16x2(__uint_as_float(a2) * oscale, __uint_as_float(a3) * oscale);
@@ -481,7 +493,7 @@ __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T
                 rank += (L2 > Lb) || (L2 == Lb && b2 < b);
             }
         }
-        order[rank] = b;
+        if (VF_IN(rank, 1, nseq, &ws->error)) order[rank] = b;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -489,6 +501,7 @@ __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T
         prefix[0] = 0;
         for (int i = 0; i < nseq; ++i) {
             const int bb = order[i];
+            if (!VF_IN(bb, 2, nseq + 1, &ws->error)) break;
             const int Lb = cu[bb + 1] - cu[bb];
             acc += ((Lb + rows_per_item - 1) / rows_per_item) * H;
             prefix[i + 1] = acc;
@@ -503,16 +516,19 @@ __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T
 namespace {
 using EncodeFn = decltype(&cuTensorMapEncodeTiled);
 
+// cuTensorMapEncodeTiled from the driver, looked up once per process (the
+// function-local static is initialised once, thread-safely); null if the
+// driver does not provide it.
 EncodeFn get_encode_fn() {
-    static EncodeFn fn = nullptr;
-    if (!fn) {
+    static const EncodeFn fn = []() -> EncodeFn {
         cudaDriverEntryPointQueryResult q;
         void* ptr = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFn>(ptr);
-    }
+            return reinterpret_cast<EncodeFn>(ptr);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -529,6 +545,10 @@ bool make_map_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+// The kernel's dynamic shared memory (above the 48 KB default) is opted into
+// once per device: the attribute belongs to the current device.
+PerDeviceOnce g_smem_attr;
 }  // namespace
 
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
@@ -557,13 +577,13 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
 
     if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, ws, s) != cudaSuccess) return VITFP8_ERR_CUDA;
 
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return VITFP8_ERR_CUDA;
-        attr_set = true;
-    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VITFP8_ERR_CUDA;
+    if (!g_smem_attr.run(dev, [] {
+            return cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES) == cudaSuccess;
+        }))
+        return VITFP8_ERR_CUDA;
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     AttnParams prm;
     prm.cu = cu;
@@ -576,9 +596,11 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     prm.T = T;
     prm.H = H;
     prm.D = D;
+    prm.Dp = Dp;
     prm.DV = DV;
     prm.KS = (D + 31) / 32;
     prm.sm_scale = sm_scale;
+    prm.out_elems = int64_t(T) * H * D;
     const long long grid = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H;
     if (grid > 0x7FFFFFFFLL) return VITFP8_ERR_UNSUPPORTED;
     attn_fp8_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);

@@ -14,6 +14,7 @@ struct SrcDev {
     int64_t s_max;
     int64_t ts;  // token stride, elements
     int64_t hs;  // head stride, elements
+    int64_t extent;  // elements the layout addresses (checked build)
 };
 
 // Attention workspace header (device), followed by int32 order[num_seqs] and
@@ -48,8 +49,11 @@ cudaError_t launch_quant(const vitfp8_scale_state* st, const uint16_t* q, const 
                          int D, int Dp, uint8_t* q8, uint8_t* k8, uint8_t* v8t, int64_t Tv,
                          cudaStream_t s);
 
-// ---- launchers (attn_fp8.cu)
+// ---- launchers (selftest.cu)
 cudaError_t launch_selftest_wait(void* ws, cudaStream_t s);
+cudaError_t launch_selftest_bounds(void* ws, cudaStream_t s);
+
+// ---- launchers (attn_fp8.cu)
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
                              void* ws, cudaStream_t s);
 vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,

@@ -8,8 +8,11 @@
 //
 // Both kernels are HBM-bound streams: 16-byte vector loads of 8 bf16 values,
 // coalesced along the head dim, tiles of 64 tokens x one head per block.
+// Every computed index passes VF_IN (checked.cuh): a no-op in the normal
+// build, a bounds check into the device error word in the checked build.
 #include <cuda_runtime.h>
 
+#include "checked.cuh"
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -29,8 +32,10 @@ __device__ __forceinline__ int64_t src_row_of(const SrcDev& L, const int32_t* cu
     int lo = 0, hi = nseq - 1;  // largest b with cu[b] <= t
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
+        if (!VF_IN(mid, 1, nseq + 1, err)) return -1;
         if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
     }
+    if (!VF_IN(lo, 1, nseq + 1, err)) return -1;
     int64_t i = int64_t(t) - __ldg(cu + lo);
     if (i < 0 || i >= L.s_max) {
         record_error(err, VITFP8_ERR_BAD_SEQLENS);
@@ -121,6 +126,7 @@ __device__ void ring_push_scale(vitfp8_scale_state* st, const float (&a)[3]) {
     const bool delayed = st->mode == 2;
     if (delayed) scale_from_ring(st);
     const int pos = st->pos;
+    if (!VF_IN(pos, 1, VITFP8_RING, &st->dev_error)) return;
     for (int t = 0; t < 3; ++t) {
         st->amax_cur[t] = a[t];
         st->hist[t][pos] = a[t];
@@ -142,7 +148,8 @@ __device__ __forceinline__ void amax_block_finish(vitfp8_scale_state* st, int z,
                                                   float* out, uint32_t* wmax) {
     m = max(m & 0xFFFFu, m >> 16);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    if ((threadIdx.x & 31) == 0 && VF_IN(threadIdx.x >> 5, 1, QT_THREADS / 32, &st->dev_error))
+        wmax[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x != 0) return;
 
@@ -183,7 +190,8 @@ amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16
             const uint16_t* __restrict__ v, SrcDev L, const int32_t* __restrict__ cu, int nseq,
             int T, int H, int D, float* __restrict__ out) {
     if (st->mode == 1) {  // static mode: nothing to track
-        if (out && threadIdx.x < 4 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        if (out && threadIdx.x < 4 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+            VF_IN(threadIdx.x, 1, 4, &st->dev_error))
             out[threadIdx.x] = 0.0f;
         return;
     }
@@ -212,6 +220,8 @@ amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16
             const int tt = i / VD;
             const int c = i - tt * VD;
             ok[u] = i < nvec && rows[tt < QT_TOK ? tt : 0] >= 0;
+            if (ok[u]) ok[u] = VF_IN(tt, 1, QT_TOK, &st->dev_error) &&
+                               VF_IN(rows[tt] * L.ts + hoff + c * 8, 8, L.extent, &st->dev_error);
             w[u] = ok[u] ? ld_stream16(src + rows[tt] * L.ts + hoff + c * 8) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -238,7 +248,9 @@ amax_rows_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q,
                  const int32_t* __restrict__ cu, int nseq, int T, int H, int D,
                  float* __restrict__ out) {
     if (st->mode == 1) {
-        if (out && threadIdx.x < 4 && blockIdx.x == 0 && blockIdx.z == 0) out[threadIdx.x] = 0.0f;
+        if (out && threadIdx.x < 4 && blockIdx.x == 0 && blockIdx.z == 0 &&
+            VF_IN(threadIdx.x, 1, 4, &st->dev_error))
+            out[threadIdx.x] = 0.0f;
         return;
     }
     const int z = blockIdx.z;
@@ -264,7 +276,10 @@ amax_rows_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q,
                 uint4 w[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    w[u] = j + 32 * u < RV ? ld_stream16(p + (j + 32 * u) * 8) : make_uint4(0, 0, 0, 0);
+                    w[u] = (j + 32 * u < RV &&
+                            VF_IN(row * L.ts + int64_t(j + 32 * u) * 8, 8, L.extent, &st->dev_error))
+                               ? ld_stream16(p + (j + 32 * u) * 8)
+                               : make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     m = absmax_bf16x2(m, w[u].x);
@@ -319,8 +334,9 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
                 uint4 w[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    w[u] = srow[u] >= 0 ? ld_stream16(src + srow[u] * L.ts + int64_t(j) * 8)
-                                        : make_uint4(0, 0, 0, 0);
+                    w[u] = (srow[u] >= 0 && VF_IN(srow[u] * L.ts + int64_t(j) * 8, 8, L.extent, err))
+                               ? ld_stream16(src + srow[u] * L.ts + int64_t(j) * 8)
+                               : make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t t = r0 + tt + u;
@@ -330,7 +346,8 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
                         o.x = quant4(w[u].x, w[u].y, inv);
                         o.y = quant4(w[u].z, w[u].w, inv);
                     }
-                    *reinterpret_cast<uint2*>(dst0 + t * (int64_t(H) * Dp) + int64_t(j) * 8) = o;
+                    if (VF_IN(t * (int64_t(H) * Dp) + int64_t(j) * 8, 8, int64_t(T) * H * Dp, err))
+                        *reinterpret_cast<uint2*>(dst0 + t * (int64_t(H) * Dp) + int64_t(j) * 8) = o;
                 }
             }
         }
@@ -364,6 +381,7 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
             const int tt = i / VP;
             const int c = i - tt * VP;
             ld[u] = i < nvec && c < VD && rows[tt < QT_TOK ? tt : 0] >= 0;
+            if (ld[u]) ld[u] = VF_IN(tt, 1, QT_TOK, err) && VF_IN(rows[tt] * L.ts + hoff + c * 8, 8, L.extent, err);
             w[u] = ld[u] ? ld_stream16(src + rows[tt] * L.ts + hoff + c * 8) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -379,11 +397,11 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
             }
             if (z < 2) {
                 const int t = t0 + tt;
-                if (t < T) {
+                if (t < T && VF_IN((int64_t(t) * H + h) * Dp + c * 8, 8, int64_t(T) * H * Dp, err)) {
                     uint8_t* dst = (z == 0 ? q8 : k8) + (int64_t(t) * H + h) * Dp + c * 8;
                     *reinterpret_cast<uint2*>(dst) = o;
                 }
-            } else {
+            } else if (VF_IN(tt * SW + 2 * c, 2, QT_TOK * (MAX_DP / 4 + 1), err)) {
                 tile[tt * SW + 2 * c] = o.x;
                 tile[tt * SW + 2 * c + 1] = o.y;
             }
@@ -400,6 +418,7 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
         const int tt = tq * 4;
         const int64_t t = int64_t(t0) + tt;
         if (t >= Tv) continue;
+        if (!VF_IN((tt + 3) * SW + dq, 1, QT_TOK * (MAX_DP / 4 + 1), err)) continue;
         const uint32_t w0 = tile[(tt + 0) * SW + dq];
         const uint32_t w1 = tile[(tt + 1) * SW + dq];
         const uint32_t w2 = tile[(tt + 2) * SW + dq];
@@ -412,7 +431,8 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
                                __byte_perm(a2, a3, 0x5410), __byte_perm(a2, a3, 0x7632)};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint32_t*>(v8t + (int64_t(h) * Dp + dq * 4 + j) * Tv + t) = o[j];
+            if (VF_IN((int64_t(h) * Dp + dq * 4 + j) * Tv + t, 4, int64_t(H) * Dp * Tv, err))
+                *reinterpret_cast<uint32_t*>(v8t + (int64_t(h) * Dp + dq * 4 + j) * Tv + t) = o[j];
     }
 }
 

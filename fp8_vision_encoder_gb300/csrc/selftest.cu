@@ -1,5 +1,6 @@
-// Failure-detection self-test of the bounded wait used by every role of the
-// attention kernels (device side of vitfp8_selftest_bounded_wait).
+// Failure-detection self-tests: the bounded wait used by every role of the
+// attention kernels (device side of vitfp8_selftest_bounded_wait), and the
+// checked build's bounds check (vitfp8_selftest_bounds_check).
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -29,6 +30,27 @@ __global__ void selftest_wait_kernel(WsHeader* ws) {
 
 cudaError_t launch_selftest_wait(void* ws, cudaStream_t s) {
     selftest_wait_kernel<<<1, 32, 0, s>>>(static_cast<WsHeader*>(ws));
+    return cudaGetLastError();
+}
+
+// Self-test of the checked build's bounds check: one thread asks VF_IN
+// whether element 16 of a 16-element buffer may be accessed.  The buffer is
+// only named, never touched: in the checked build the check refuses and
+// records VITFP8_ERR_DEVICE_BOUNDS, so the access it guards is skipped; in
+// the normal build the check is compiled away and nothing is recorded.
+__global__ void selftest_bounds_kernel(WsHeader* ws) {
+    ws->error = 0;
+    const int64_t n = 16;
+    if (VF_IN(n, 1, n, &ws->error)) {
+        // The access a failed check would skip (none here).
+    }
+    if (VF_IN(0, 1, n, &ws->error)) {
+        // In range: nothing is recorded.
+    }
+}
+
+cudaError_t launch_selftest_bounds(void* ws, cudaStream_t s) {
+    selftest_bounds_kernel<<<1, 1, 0, s>>>(static_cast<WsHeader*>(ws));
     return cudaGetLastError();
 }
 

@@ -18,7 +18,15 @@
  *   - Pointers named d_* and all tensor pointers are DEVICE pointers; h_* are
  *     HOST pointers.  The caller allocates and frees every buffer (sources,
  *     codes, outputs, state, workspace).  The library never allocates or
- *     frees memory on these calls and keeps no mutable global state.
+ *     frees memory on these calls.  Its only process-wide state is set-up
+ *     that belongs to a device and is done once per device, under a lock, on
+ *     the first call that needs it: the attention kernels' opt-in to more
+ *     than 48 KB of shared memory, the driver's tensor-map encoder (looked
+ *     up once per process), and the device address of the scratch array of
+ *     vitfp8_attn_varlen_noalloc.  Every entry point may be called from
+ *     several host threads at once and for several devices in one process;
+ *     calls on one stream run in order, calls on different streams that
+ *     share a buffer must be ordered by the caller.
  *   - All work is enqueued asynchronously on `stream`; nothing synchronises
  *     with the host except vitfp8_get_device_error /
  *     vitfp8_get_workspace_error, which synchronise `stream`.
@@ -50,7 +58,7 @@ typedef enum vitfp8_status {
     VITFP8_ERR_UNSUPPORTED = 2,    /* valid request outside what the kernels cover (e.g. D > 128) */
     VITFP8_ERR_CUDA = 3,           /* a CUDA runtime / driver call failed */
     VITFP8_ERR_DEVICE_TIMEOUT = 4, /* device: a bounded wait expired; the kernel returned early */
-    VITFP8_ERR_DEVICE_BOUNDS = 5,  /* device: an index fell outside its buffer and was skipped */
+    VITFP8_ERR_DEVICE_BOUNDS = 5,  /* device (checked build): an index fell outside its buffer and was skipped */
     VITFP8_ERR_BAD_SEQLENS = 6,    /* device: cu_seqlens not 0 = c0 <= c1 <= ... <= c_B = T */
     VITFP8_ERR_WORKSPACE = 7       /* workspace missing or smaller than vitfp8_attn_workspace_size */
 } vitfp8_status;
@@ -298,7 +306,11 @@ vitfp8_status vitfp8_attn_varlen_bf16(const vitfp8_bf16* q, const vitfp8_bf16* k
  * segments: num_seqs above that returns VITFP8_ERR_UNSUPPORTED without
  * launching.  The first call on each device looks up that array's device
  * address (cudaGetSymbolAddress) with the device current; make that first
- * call before any stream capture.  Every call on a device shares the one
+ * call before any stream capture.  The address is kept for the rest of the
+ * process: after a cudaDeviceReset (or anything else that destroys the
+ * device's primary context) the library's device code is loaded anew and the
+ * kept address is stale, so do not call this entry point on that device
+ * again in the same process.  Every call on a device shares the one
  * array and rewrites all of it that it reads, so nothing carries over between
  * calls; calls that overlap on the GPU (different streams, or different
  * host threads, without ordering) race on it.  Device-detected errors
@@ -335,6 +347,29 @@ vitfp8_status vitfp8_get_workspace_error(const void* d_workspace, int32_t* h_out
  */
 vitfp8_status vitfp8_selftest_bounded_wait(void* d_workspace, size_t workspace_bytes,
                                           cudaStream_t stream);
+
+/*
+ * 1 if this library was compiled as the checked build (-DVITFP8_CHECKED),
+ * else 0.  In the checked build every global- and shared-memory index the
+ * kernels compute is compared with the extent its arguments imply (sources
+ * by their layout, codes [T, H, D_pad] and [H, D_pad, Tv], output [T, H, D],
+ * cu_seqlens and the work list by num_seqs); an index outside records
+ * VITFP8_ERR_DEVICE_BOUNDS in the call's device error word (the scale
+ * state's for amax and quantization, the workspace's for attention) and the
+ * access is skipped.  Nothing traps.  The normal build has no checks.
+ */
+int32_t vitfp8_checked_build(void);
+
+/*
+ * Self-test of that bounds check: one thread asks the check whether element
+ * 16 of a 16-element buffer may be accessed (the buffer is never touched).
+ * The checked build records VITFP8_ERR_DEVICE_BOUNDS in the workspace error
+ * word (cleared at launch); the normal build records nothing.  Read it with
+ * vitfp8_get_workspace_error.  d_workspace: at least
+ * vitfp8_attn_workspace_size(0) bytes, 4-byte aligned.
+ */
+vitfp8_status vitfp8_selftest_bounds_check(void* d_workspace, size_t workspace_bytes,
+                                           cudaStream_t stream);
 
 #ifdef __cplusplus
 }

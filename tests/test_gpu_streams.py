@@ -95,3 +95,66 @@ def test_two_layers_on_two_streams_equal_one_stream(vf):
         for f in range(FORWARDS):
             assert torch.equal(L["outs"][f], ro[f]), "forward %d differs" % f
         assert st.device_error() == 0 and L["ws"].error() == 0
+
+
+def test_attention_from_two_host_threads(vf):
+    """Two host threads, each driving FP8 and BF16 attention on its own stream
+    with its own workspace, at the same time (the binding's ctypes calls
+    release the GIL, so the library's host code runs concurrently, including
+    its once-per-device set-up when these are the process's first attention
+    calls): every output is bit-identical to the same call made alone."""
+    import threading
+
+    cases = [([900, 300], 4, 128, 701), ([1500, 64, 700], 2, 80, 702)]
+    prepared = []
+    for seqlens, H, D, seed in cases:
+        cu, _ = cu_tensor(seqlens)
+        q, k, v = qkv(seqlens, H, D, seed)
+        st = vf.ScaleState().init()
+        vf.amax_update(st, q, k, v, cu)
+        q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
+        prepared.append(dict(seqlens=seqlens, D=D, cu=cu, q=q, k=k, v=v, st=st,
+                             q8=q8, k8=k8, v8t=v8t))
+    torch.cuda.synchronize()
+
+    results = [dict() for _ in prepared]
+    errors = []
+    streams = [torch.cuda.Stream() for _ in prepared]
+    start = threading.Barrier(len(prepared))
+    REPS = 12
+
+    def run(i):
+        P = prepared[i]
+        try:
+            torch.cuda.set_device(0)
+            ws = vf.Workspace(len(P["seqlens"]))
+            s = streams[i]
+            fp8 = [torch.empty_like(P["q"]) for _ in range(REPS)]
+            bf16 = [torch.empty_like(P["q"]) for _ in range(REPS)]
+            start.wait()
+            for r in range(REPS):
+                vf.attn_varlen(P["q8"], P["k8"], P["v8t"], P["st"], P["cu"], max(P["seqlens"]),
+                               P["D"], out=fp8[r], workspace=ws, stream=s)
+                vf.attn_varlen_bf16(P["q"], P["k"], P["v"], P["cu"], max(P["seqlens"]),
+                                    out=bf16[r], workspace=ws, stream=s)
+            s.synchronize()
+            results[i] = dict(fp8=fp8, bf16=bf16, err=ws.error(stream=s))
+        except Exception as e:  # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(len(prepared))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not errors, errors
+    assert all(not t.is_alive() for t in threads)
+
+    for P, R in zip(prepared, results):
+        ref8 = vf.attn_varlen(P["q8"], P["k8"], P["v8t"], P["st"], P["cu"], max(P["seqlens"]), P["D"])
+        ref16 = vf.attn_varlen_bf16(P["q"], P["k"], P["v"], P["cu"], max(P["seqlens"]))
+        torch.cuda.synchronize()
+        assert R["err"] == 0
+        for r in range(REPS):
+            assert torch.equal(R["fp8"][r].view(torch.int16), ref8.view(torch.int16)), "fp8 rep %d" % r
+            assert torch.equal(R["bf16"][r].view(torch.int16), ref16.view(torch.int16)), "bf16 rep %d" % r

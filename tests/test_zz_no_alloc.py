@@ -70,3 +70,25 @@ def test_noalloc_rejects_too_many_segments():
     assert _call_noalloc(vf, q8, k8, v8t, st, cu, 1, 64, out) == 2   # VITFP8_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert torch.all(out == 0)
+
+
+def test_noalloc_after_a_call_with_malformed_seqlens():
+    """A call whose device-side check fails (non-monotonic cu_seqlens) leaves
+    its output unwritten and puts "no work" into the shared scratch; the next
+    valid call must still compute everything, bit-identical to the workspace
+    entry point."""
+    import fp8_vision_encoder_gb300 as vf
+    seqlens, H, D = [300, 129, 500], 2, 128
+    cu, st, q8, k8, v8t = _inputs(vf, seqlens, H, D, 34)
+    T = sum(seqlens)
+    bad = torch.tensor([0, 400, 300, T], dtype=torch.int32, device="cuda")  # 400 > 300
+    out_bad = torch.full((T, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(vf, q8, k8, v8t, st, bad, max(seqlens), D, out_bad) == 0
+    torch.cuda.synchronize()
+    assert torch.isnan(out_bad.float()).all(), "the rejected call wrote output"
+
+    ref = vf.attn_varlen(q8, k8, v8t, st, cu, max(seqlens), D)
+    out = torch.full((T, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(vf, q8, k8, v8t, st, cu, max(seqlens), D, out) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
