@@ -193,32 +193,70 @@ def test_bad_seqlens_padded_sets_error_not_fault(vf):
     assert st.device_error() == 6
 
 
-@pytest.mark.parametrize("name", ["micro8k", "uhd3mix"])
-def test_full_size_codes_sampled_and_amax_exact(vf, name):
+def _oracle_code_table(inv):
+    """E4M3 code of float32(x) * inv for every bf16 bit pattern x, from the
+    oracle's quantize (the code of an element depends on nothing else)."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    x = (bits << 16).view(np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        return oquant.quantize(x, inv)
+
+
+def _assert_codes_full(codes_thd, x, inv, chunk=1 << 14):
+    """Every code of a [T, H, D] (or strided [T, H, D_pad] view) against the
+    oracle, in token chunks so host memory stays bounded."""
+    table = _oracle_code_table(inv)
+    T = x.shape[0]
+    for t0 in range(0, T, chunk):
+        xb = x[t0:t0 + chunk].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        got = codes_thd[t0:t0 + chunk].cpu().numpy()
+        ref = table[xb]
+        mism = np.count_nonzero(got != ref)
+        assert mism == 0, "%d code mismatches in tokens %d.." % (mism, t0)
+
+
+@pytest.mark.parametrize("name", ["micro8k", "qhd3", "uhd3mix"])
+def test_full_size_codes_and_amax_exact(vf, name):
+    """Full-size workloads: the scale state bit-exact with the oracle's, and
+    EVERY code of q, k and v (all T x H x D of each, V through its transposed
+    layout) equal to the oracle's quantization of its bf16 input.  qhd3 runs
+    as the bench runs it: 16 dynamic calibration forwards, static scales
+    1.5 x the calibrated amax, one layer."""
     w = workloads.WORKLOADS[name]
     cu, cul = cu_tensor(w.seqlens)
-    seed = w.seeds[0]
-    q, k, v = [t for t in workloads.make_qkv(w.seqlens, w.H, w.D, seed, w.outliers, w.per_head_std,
-                                             device="cuda")]
+    gen = lambda seed: workloads.make_qkv(w.seqlens, w.H, w.D, seed, w.outliers, w.per_head_std,
+                                          device="cuda")
     st = vf.ScaleState().init()
     ost = oscales.ScaleState()
-    if w.static:
+    if w.scaling == "static":
         st.set_static(*w.static)
         ost.set_static(*w.static)
+        q, k, v = gen(w.seeds[0])
+    elif w.scaling == "calibrated":
+        for seed in w.calib_seeds:
+            q, k, v = gen(seed)
+            vf.amax_update(st, q, k, v, cu)
+            oracle_push(ost, q, k, v)
+        state_matches(st.read(), ost)
+        A = [float(np.float32(a) * np.float32(1.5)) for a in ost.amax_ref]
+        st.set_static(*A)
+        ost.set_static(*A)
+        q, k, v = gen(w.layer_seeds[0])
     else:
+        q, k, v = gen(w.seeds[0])
         vf.amax_update(st, q, k, v, cu)
         oracle_push(ost, q, k, v)
     state_matches(st.read(), ost)
     q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
     torch.cuda.synchronize()
-    rows = torch.from_numpy(np.random.default_rng(0).choice(w.T, 3000, replace=False)).cuda()
-    rows = torch.cat([rows, torch.tensor([0, w.T - 1], device="cuda")])
-    vthd = v8t[:, :, :w.T]
-    for t, (codes, x) in enumerate(((q8, q), (k8, k), (None, v))):
-        xs = x[rows]
-        got = codes[rows] if codes is not None else vthd[:, :, rows].permute(2, 0, 1)
-        ref = oquant.quantize(np32(xs), ost.inv_scale[t])
-        assert np.array_equal(got.cpu().numpy(), ref)
+    assert st.device_error() == 0
+    D = w.D
+    _assert_codes_full(q8[:, :, :D], q, ost.inv_scale[0])
+    _assert_codes_full(k8[:, :, :D], k, ost.inv_scale[1])
+    _assert_codes_full(v8t[:, :D, :w.T].permute(2, 0, 1), v, ost.inv_scale[2])
+    # head-dim padding and V's token padding are zero codes
+    if q8.shape[2] > D:
+        assert int(q8[:, :, D:].sum().item()) == 0 and int(k8[:, :, D:].sum().item()) == 0
 
 
 @pytest.mark.parametrize("split", [False, True])
