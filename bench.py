@@ -48,6 +48,12 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+# Source files each profiled kernel is compiled from (the summaries under
+# profiles/ record a hash over them).
+ATTN_FP8_SOURCES = ["attn_fp8.cu", "attn_common.cuh", "checked.cuh", "ptx.cuh"]
+QUANT_SOURCES = ["quant.cu", "checked.cuh", "internal.cuh", "ptx.cuh"]
+
+
 def _profile_traffic(md_name, sources):
     """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged."""
     import hashlib
@@ -310,12 +316,13 @@ SWEEP_SIZES = [("HD 720x1280", 45 * 80), ("FullHD 1080x1920", 67 * 120),
                ("QHD 1440x2560", 90 * 160), ("4K 2160x3840", 135 * 240)]
 
 
-def resolution_sweep(vf, dev, stream, reps, head_dims=(80, 128), H=16, images=3):
+def resolution_sweep(vf, dev, stream, reps, head_dims=(80, 128), H=16, images=3, echo=True):
     """One attention layer per image size: FP8 with dynamic scaling (amax +
     quant + attention), FP8 with static scales (quant + attention) and the BF16
     path, each timed alone with CUDA events and L2 flushed before every rep;
-    prints one JSON line per (size, head_dim)."""
+    returns (and with ``echo`` prints) one record per (size, head_dim)."""
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rows = []
     for D in head_dims:
         for name, L in SWEEP_SIZES:
             seqlens = [L] * images
@@ -354,13 +361,98 @@ def resolution_sweep(vf, dev, stream, reps, head_dims=(80, 128), H=16, images=3)
                 res[arm] = statistics.median(times)
             assert wsp.error() == 0
             flops = 4 * images * L * L * H * D
-            print(json.dumps({
+            row = {
                 "sweep": name, "tokens_per_image": L, "images": images, "heads": H, "head_dim": D,
                 **{k2 + "_us": round(v2, 1) for k2, v2 in res.items()},
                 "fp8_dynamic_vs_bf16": round(res["bf16"] / res["fp8_dynamic"], 3),
                 "fp8_static_vs_bf16": round(res["bf16"] / res["fp8_static"], 3),
                 "fp8_attn_tflops": round(flops / res["fp8_attn_only"] / 1e6, 1),
-                "bf16_tflops": round(flops / res["bf16"] / 1e6, 1)}), flush=True)
+                "bf16_tflops": round(flops / res["bf16"] / 1e6, 1)}
+            rows.append(row)
+            if echo:
+                print(json.dumps(row), flush=True)
+            del q, k, v, codes, out
+    return rows
+
+
+# The other configurations of the workload list, reported beside the headline
+# one (which sets `value`): tiny packed varlen, the 8192-token kernel
+# microbench, 3 HD images at d = 80 and 3 4K images plus mixed segments.
+PER_CONFIG = ["tiny", "micro8k", "hd3", "uhd3mix"]
+
+
+def per_config_block(vf, dev, stream, peaks, peak_kind, reps=None):
+    """One layer of each PER_CONFIG workload as `bench.py --workload NAME` runs
+    it (dynamic scaling = amax + ring + quantize; static = quantize), FP8
+    attention and the BF16 path on the same inputs; each arm timed alone with
+    CUDA events, the L2 flushed (a 256 MB write, outside the timed span) before
+    every rep, median of the reps."""
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    bf16_peak = peaks["bf16_tflops_sustained"]
+    block = {}
+    for name in PER_CONFIG:
+        w = workloads.WORKLOADS[name]
+        run = Runner(vf, w, dev, layers=1)
+        q, k, v = run.inputs[0]
+        st = run.states[0]
+        q8, k8, v8t = run.codes
+
+        def quant():
+            if run.dynamic:
+                vf.amax_update(st, q, k, v, run.cu, stream=stream)
+            vf.quantize_unpad(st, q, k, v, run.cu, D_pad=run.D_pad, out=run.codes, stream=stream)
+
+        arms = {
+            "quant": quant,
+            "fp8_attn": lambda: vf.attn_varlen(q8, k8, v8t, st, run.cu, w.max_seqlen, w.D,
+                                               out=run.out, workspace=run.ws, stream=stream),
+            "bf16_attn": lambda: vf.attn_varlen_bf16(q, k, v, run.cu, w.max_seqlen, out=run.out,
+                                                     workspace=run.ws, stream=stream),
+        }
+        n = reps if reps is not None else (5 if w.flops() > 1e13 else 15)
+        res = {}
+        for arm, fn in arms.items():
+            for _ in range(3):
+                fn()
+            times = []
+            for _ in range(n):
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                times.append(e0.elapsed_time(e1) * 1e3)
+            res[arm] = statistics.median(times)
+        assert run.ws.error() == 0 and st.device_error() == 0
+        flops = w.flops()
+        qbytes = _quant_bytes(w, run.dynamic)
+        fp8_tf = flops / res["fp8_attn"] / 1e6
+        bf16_tf = flops / res["bf16_attn"] / 1e6
+        layer_us = res["quant"] + res["fp8_attn"]
+        block[name] = {
+            "workload": w.desc, "scaling": "dynamic" if run.dynamic else "static",
+            "tokens": w.T, "heads": w.H, "head_dim": w.D, "flops": flops,
+            "fp8_attn_us": round(res["fp8_attn"], 1), "fp8_attn_tflops": round(fp8_tf, 1),
+            "fp8_attn_frac_of_peak": round(fp8_tf / fp8_peak, 4),
+            "quant_us": round(res["quant"], 1), "quant_bytes": qbytes,
+            "quant_gbs": round(qbytes / res["quant"] / 1e3, 1),
+            "quant_frac_of_hbm": round(qbytes / res["quant"] / 1e3 / peaks["hbm_gbs"], 4),
+            "layer_us": round(layer_us, 1), "layer_tflops_incl_quant": round(flops / layer_us / 1e6, 1),
+            "bf16_attn_us": round(res["bf16_attn"], 1), "bf16_tflops": round(bf16_tf, 1),
+            "bf16_frac_of_peak": round(bf16_tf / bf16_peak, 4),
+            "fp8_vs_bf16_attn": round(res["bf16_attn"] / res["fp8_attn"], 3),
+            "fp8_with_quant_vs_bf16": round(res["bf16_attn"] / layer_us, 3),
+            "reps": n}
+        del run, q, k, v, q8, k8, v8t, st
+        torch.cuda.empty_cache()
+    block["_peaks"] = {"fp8": fp8_peak, "bf16": bf16_peak, "hbm_gbs": peaks["hbm_gbs"],
+                       "source": "%s bf16 sustained x %.0f for FP8; %s HBM copy"
+                                 % (peak_kind, FP8_PER_BF16, peak_kind),
+                       "l2": "flushed (256 MB write) before every rep, outside the timed span"}
+    return block
 
 
 def main():
@@ -374,7 +466,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison column")
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload block and the resolution sweep block")
     ap.add_argument("--sweep", action="store_true",
                help="per image size: FP8 (dynamic / static, with quant) vs BF16 layer time, then exit")
     ap.add_argument("--sweep-reps", type=int, default=7)
@@ -492,8 +586,7 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "attn_fp8 (work-list + attention launch)",
                      "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp8_peak,
-                     "traffic": (_profile_traffic("attn_fp8_qhd3.md",
-                                                  ["attn_fp8.cu", "attn_common.cuh", "ptx.cuh"])
+                     "traffic": (_profile_traffic("attn_fp8_qhd3.md", ATTN_FP8_SOURCES)
                                  if w.name == "qhd3" else None),
                      "algorithmic_bytes": 3 * w.T * w.H * w.D + 2 * w.T * w.H * w.D,
                      "peak_source": "%s bf16 sustained x %.0f (fp8/bf16 nominal ratio)"
@@ -501,7 +594,7 @@ def main():
         "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": quant_gbs / peaks["hbm_gbs"],
                            "algorithmic_bytes": qbytes, "peak_source": peak_kind,
-                           "traffic": (_profile_traffic("quant_qhd3.md", ["quant.cu", "ptx.cuh"])
+                           "traffic": (_profile_traffic("quant_qhd3.md", QUANT_SOURCES)
                                        if w.name == "qhd3" and not run.dynamic else None)},
         "breakdown_us": {"quant": 1e3 * quant_avg, "attn": 1e3 * attn_avg},
         "gpu_launches": run.launches_layer * run.layers * args.steps,
@@ -516,6 +609,13 @@ def main():
     # end to end through the public API with host buffers
     if not args.no_e2e:
         line["e2e"] = e2e(vf, run, stream, dev, args.e2e_steps, max(3, args.warmup), ws, pg)
+    # The other workloads and the resolution sweep, beside the headline line
+    # (one GPU; after the timed region, so they do not touch its numbers).
+    if rank == 0 and ws == 1 and not args.no_per_config and args.workload == "qhd3":
+        del run.inputs
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config_block(vf, dev, stream, peaks, peak_kind)
+        line["sweep"] = resolution_sweep(vf, dev, stream, reps=5, echo=False)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, cores, desc, dt = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -664,14 +764,14 @@ def e2e(vf, run, stream, dev, steps, warmup, ws, pg):
                         s_out)
     if pg:
         pg.barrier()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    marks[0].record(stream)
+    for i in range(steps):
         one_step()
-    b.record(stream)
+        marks[i + 1].record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b)
+    ms = marks[0].elapsed_time(marks[-1])
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
     if pg:
         t = torch.tensor([ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -679,6 +779,7 @@ def e2e(vf, run, stream, dev, steps, warmup, ws, pg):
     val = ws * run.flops_layer * run.layers * steps / (ms * 1e-3) / 1e12
     return {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
+            "step_ms": [round(x, 2) for x in step_ms],
             "link_gbs": {"h2d": h2d_link, "d2h": d2h_link,
                          "step_floor_ms": h2d / (h2d_link * 1e6)},
             "copies": "pinned host buffers; H2D, compute and D2H on three streams, overlapped across layers"}

@@ -119,6 +119,8 @@ _attn_bf16 = _sig("vitfp8_attn_varlen_bf16", ctypes.c_int,
                    _vp])
 NOALLOC_MAX_SEQS = 4096
 _selftest_wait = _sig("vitfp8_selftest_bounded_wait", ctypes.c_int, [_vp, ctypes.c_size_t, _vp])
+_calibrated = _sig("vitfp8_calibrated_scales", ctypes.c_int,
+                   [_vp, ctypes.c_float, _vp, _vp, _vp])
 _selftest_bounds = _sig("vitfp8_selftest_bounds_check", ctypes.c_int, [_vp, ctypes.c_size_t, _vp])
 _checked_build = _sig("vitfp8_checked_build", ctypes.c_int32, [])
 _get_err = _sig("vitfp8_get_device_error", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
@@ -324,6 +326,18 @@ class Workspace:
         _check(_get_ws_err(_ptr(self.buf), ctypes.byref(out), _stream(stream)),
                "vitfp8_get_workspace_error")
         return out.value
+
+
+def calibrated_scales(dynamic_state, margin=1.5, static_state=None, stream=None):
+    """Saved scale-file values float32(A) * float32(margin) of a calibrated
+    dynamic state (A = its ring maximum per tensor), computed on the device;
+    returns a device float32 tensor [3] (q, k, v).  With ``static_state`` that
+    state is also set to static mode with those values."""
+    out = torch.empty(3, dtype=torch.float32, device=dynamic_state.buf.device)
+    _check(_calibrated(dynamic_state.ptr, float(margin), _ptr(out),
+                       static_state.ptr if static_state is not None else None, _stream(stream)),
+           "vitfp8_calibrated_scales")
+    return out
 
 
 def checked_build():

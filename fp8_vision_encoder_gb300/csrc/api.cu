@@ -137,6 +137,19 @@ vitfp8_status vitfp8_ring_push(vitfp8_scale_state* d_state, const float* d_vals,
     return launch_ring_push(d_state, d_vals, stream) == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
 }
 
+vitfp8_status vitfp8_calibrated_scales(const vitfp8_scale_state* d_dynamic, float margin,
+                                       float* d_saved, vitfp8_scale_state* d_static,
+                                       cudaStream_t stream) {
+    if (!d_dynamic || !aligned4(d_dynamic)) return VITFP8_ERR_INVALID_ARG;
+    if (!std::isfinite(margin) || !(margin > 0.0f)) return VITFP8_ERR_INVALID_ARG;
+    if (d_saved && !aligned4(d_saved)) return VITFP8_ERR_INVALID_ARG;
+    if (d_static && !aligned4(d_static)) return VITFP8_ERR_INVALID_ARG;
+    if (d_static == d_dynamic) return VITFP8_ERR_INVALID_ARG;
+    return launch_calibrated_scales(d_dynamic, margin, d_saved, d_static, stream) == cudaSuccess
+               ? VITFP8_OK
+               : VITFP8_ERR_CUDA;
+}
+
 int64_t vitfp8_vt_stride(int32_t total_tokens) {
     if (total_tokens < 0) return 0;
     return (int64_t(total_tokens) + 15) & ~int64_t(15);

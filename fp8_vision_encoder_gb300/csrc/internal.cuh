@@ -43,6 +43,8 @@ cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_
                         const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
                         int D, float* out, cudaStream_t s);
 cudaError_t launch_ring_push(vitfp8_scale_state* st, const float* vals, cudaStream_t s);
+cudaError_t launch_calibrated_scales(const vitfp8_scale_state* dyn, float margin, float* out,
+                                     vitfp8_scale_state* dst, cudaStream_t s);
 cudaError_t launch_set_ring_order(vitfp8_scale_state* st, int delayed, cudaStream_t s);
 cudaError_t launch_quant(const vitfp8_scale_state* st, const uint16_t* q, const uint16_t* k,
                          const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,

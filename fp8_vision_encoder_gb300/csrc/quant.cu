@@ -436,6 +436,39 @@ quant_kernel(const vitfp8_scale_state* __restrict__ st, const uint16_t* __restri
     }
 }
 
+// ---------------------------------------------------------------- calibrate once
+
+// Calibrate-once step on the device: for each tensor the ring maximum A of
+// the calibrated dynamic state, the saved value float32(A) * float32(margin)
+// written to `out` (if given), and the static state `dst` (if given) set from
+// those values exactly as vitfp8_set_static_scales would.  A tensor whose ring
+// holds no amax (A == 0) makes no valid static scale: the dynamic state's
+// error word records VITFP8_ERR_INVALID_ARG and `dst` is left as it is.  One
+// thread.
+__global__ void calibrated_scales_kernel(vitfp8_scale_state* dyn, float margin, float* out,
+                                         vitfp8_scale_state* dst) {
+    float saved[3];
+    bool ok = true;
+    for (int t = 0; t < 3; ++t) {
+        float A = 0.0f;
+        for (int i = 0; i < VITFP8_RING; ++i) A = fmaxf(A, dyn->hist[t][i]);
+        saved[t] = __fmul_rn(A, margin);
+        ok = ok && saved[t] > 0.0f && saved[t] <= 3.4028234e38f;
+        if (out) out[t] = saved[t];
+    }
+    if (!ok) {
+        record_error(&dyn->dev_error, VITFP8_ERR_INVALID_ARG);
+        return;
+    }
+    if (dst) {
+        dst->mode = 1;
+        for (int t = 0; t < 3; ++t) {
+            dst->amax_ref[t] = saved[t];
+            scale_from_amax(saved[t], dst->scale[t], dst->inv_scale[t]);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- launchers
 
 cudaError_t launch_state_init(vitfp8_scale_state* st, cudaStream_t s) {
@@ -465,6 +498,12 @@ cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_
 
 cudaError_t launch_set_ring_order(vitfp8_scale_state* st, int delayed, cudaStream_t s) {
     set_ring_order_kernel<<<1, 1, 0, s>>>(st, delayed);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_calibrated_scales(const vitfp8_scale_state* dyn, float margin, float* out,
+                                     vitfp8_scale_state* dst, cudaStream_t s) {
+    calibrated_scales_kernel<<<1, 1, 0, s>>>(const_cast<vitfp8_scale_state*>(dyn), margin, out, dst);
     return cudaGetLastError();
 }
 

@@ -349,6 +349,30 @@ vitfp8_status vitfp8_selftest_bounded_wait(void* d_workspace, size_t workspace_b
                                           cudaStream_t stream);
 
 /*
+ * Calibrate once, on the device ("FP8 ViT Encoder Attention", Calibrate-Once,
+ * Reuse Workflow; Scale File Format; "FP8 vision encoder attention" (Sonar),
+ * Create static scales): after the calibration forwards (16 on the pages) of
+ * a layer in dynamic mode, take each tensor's learned scale -- its ring
+ * maximum A, whatever the ring order -- and the value the scale file saves,
+ * float32(A) * float32(margin) (one float32 multiply; the pages' default
+ * margin is 1.5).
+ *
+ * d_dynamic: the calibrated state (device, read only except its error word).
+ * margin: finite, > 0 (else VITFP8_ERR_INVALID_ARG before any launch).
+ * d_saved: optional device float[3], receives the saved values (q, k, v),
+ *   which a caller copies back to write the scale file.
+ * d_static: optional device state, set to static mode with the saved values
+ *   exactly as vitfp8_set_static_scales would; must not be d_dynamic.
+ * A tensor whose ring holds no amax (A == 0) has no valid static scale: the
+ * dynamic state's error word records VITFP8_ERR_INVALID_ARG (read it with
+ * vitfp8_get_device_error) and d_static is left unchanged.  Stream-ordered,
+ * one launch, no host synchronisation.
+ */
+vitfp8_status vitfp8_calibrated_scales(const vitfp8_scale_state* d_dynamic, float margin,
+                                       float* d_saved, vitfp8_scale_state* d_static,
+                                       cudaStream_t stream);
+
+/*
  * 1 if this library was compiled as the checked build (-DVITFP8_CHECKED),
  * else 0.  In the checked build every global- and shared-memory index the
  * kernels compute is compared with the extent its arguments imply (sources

@@ -7,8 +7,10 @@
  *
  * IN:  int32 T, H, D, nseq, forwards; int32 cu_seqlens[nseq + 1]; then for
  *      each forward bf16 q, k, v, each [T][H][D] (raw 16-bit patterns).
- * OUT: the vitfp8_scale_state after the last forward (raw bytes), then the
- *      bf16 attention output [T][H][D] of the last forward.
+ * OUT: the vitfp8_scale_state after the last forward (raw bytes), the bf16
+ *      attention output [T][H][D] of the last forward, then the three
+ *      scale-file values (float32, q k v) vitfp8_calibrated_scales gives for
+ *      that state with margin 1.5.
  *
  * Each forward runs dynamic scaling, quantization with un-padding and FP8
  * attention on one stream.  Every status is checked; the exit code is 0 only
@@ -100,6 +102,13 @@ int main(int argc, char** argv) {
     }
     fclose(in);
 
+    /* Calibrate once from C: the scale-file values of this state (margin 1.5). */
+    float* d_saved;
+    float h_saved[3];
+    CK_CUDA(cudaMalloc((void**)&d_saved, 3 * sizeof(float)));
+    CK_VF(vitfp8_calibrated_scales(d_state, 1.5f, d_saved, NULL, s));
+    CK_CUDA(cudaMemcpyAsync(h_saved, d_saved, sizeof(h_saved), cudaMemcpyDeviceToHost, s));
+
     int32_t dev_err = -1, ws_err = -1;
     CK_VF(vitfp8_get_device_error(d_state, &dev_err, s));
     CK_VF(vitfp8_get_workspace_error(d_ws, &ws_err, s));
@@ -109,7 +118,8 @@ int main(int argc, char** argv) {
     FILE* out = fopen(argv[2], "wb");
     if (!out) return 1;
     if (fwrite(&h_state, sizeof(h_state), 1, out) != 1 ||
-        fwrite(h_out, sizeof(vitfp8_bf16), n_elem, out) != n_elem)
+        fwrite(h_out, sizeof(vitfp8_bf16), n_elem, out) != n_elem ||
+        fwrite(h_saved, sizeof(float), 3, out) != 3)
         return 1;
     fclose(out);
     printf("vitfp8 %d: device error %d, workspace error %d\n", vitfp8_version(), dev_err, ws_err);

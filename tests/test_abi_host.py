@@ -111,6 +111,18 @@ def test_validation_rejects_without_launch(vf):
     assert call(ws=P(0)) == 7
     assert call(wsb=ws - 1) == 7
     assert call(nseq=0, T=0) == 0              # empty: no-op
+    # calibrate once: margin must be finite and positive, the static state distinct
+    cs = vf._calibrated
+    assert cs(P(0), 1.5, P(0), P(0), P(0)) == 1
+    assert cs(good, 0.0, P(0), P(0), P(0)) == 1
+    assert cs(good, float("nan"), P(0), P(0), P(0)) == 1
+    assert cs(good, float("inf"), P(0), P(0), P(0)) == 1
+    assert cs(good, 1.5, P((1 << 20) + 2), P(0), P(0)) == 1   # d_saved not 4-byte aligned
+    assert cs(good, 1.5, P(0), good, P(0)) == 1     # d_static == d_dynamic
+    # self-test arguments
+    assert vf._selftest_bounds(P(0), 256, P(0)) == 1
+    assert vf._selftest_bounds(good, 8, P(0)) == 1
+    assert vf._checked_build() in (0, 1)
 
 
 def test_oracle_and_product_share_no_code():

@@ -1,8 +1,9 @@
 """GPU: the library driven from plain C through its ABI alone.
 
 tests/c_client/vitfp8_client.c allocates with cudaMalloc, runs dynamic
-scaling, quantization and attention for a few forwards and writes the scale
-state and the output; both are compared with the oracle.
+scaling, quantization and attention for a few forwards, takes the
+calibrate-once scale-file values of the state on the device, and writes the
+scale state, the output and those values; all are compared with the oracle.
 """
 
 import math
@@ -15,7 +16,7 @@ import pytest
 import torch
 
 import workloads
-from oracle import quant as oquant, scales as oscales
+from oracle import calib as ocalib, quant as oquant, scales as oscales
 
 from gpu_util import assert_attention_ok, compare_attention, np32, oracle_push, state_matches
 
@@ -67,8 +68,14 @@ def test_plain_c_client_matches_oracle(tmp_path):
              "inv_scale": list(s.inv_scale), "amax_cur": list(s.amax_cur),
              "amax_bits": list(s.amax_bits), "blocks_done": s.blocks_done, "dev_error": s.dev_error}
     state_matches(state, ost)
-    out = torch.from_numpy(np.frombuffer(raw[nst:], dtype=np.int16).copy()).view(torch.bfloat16)
+    nout = T * H * D * 2
+    out = torch.from_numpy(np.frombuffer(raw[nst:nst + nout], dtype=np.int16).copy()).view(torch.bfloat16)
     out = out.reshape(T, H, D)
+    # calibrate-once from C: float32(ring max) * float32(1.5), bit for bit
+    saved = np.frombuffer(raw[nst + nout:nst + nout + 12], dtype=np.float32)
+    want = np.asarray(ocalib.saved_values(np.asarray(ost.hist, dtype=np.float32).max(axis=1), 1.5),
+                      dtype=np.float32)
+    assert np.array_equal(saved.view(np.uint32), want.view(np.uint32)), (saved, want)
     # oracle codes of the last forward (bit-exact with the library's, checked elsewhere)
     codes = [torch.from_numpy(oquant.quantize(np32(x), ost.inv_scale[t]))
              for t, x in enumerate((q, k, v))]

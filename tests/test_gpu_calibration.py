@@ -135,3 +135,50 @@ def test_dynamic_forward_replays_from_one_cuda_graph(vf):
     state_matches(st.read(), ost)
     stats = compare_attention(out, codes[0], codes[1], vt_to_thd(codes[2], T), list(ost.scale), cul, D)
     assert_attention_ok(stats, "graph replay", outliers=True)
+
+
+@pytest.mark.parametrize("delayed", [False, True])
+def test_device_calibrated_scales_match_oracle(vf, delayed):
+    """vitfp8_calibrated_scales: after 16 dynamic forwards, the saved values
+    float32(ring max) * float32(margin) come out of the device bit-exact with
+    the oracle's, for several margins and either ring order, and the static
+    state it sets equals the oracle's static state from those values."""
+    seqlens, H, D = [300, 77, 500], 4, 128
+    cu, _ = cu_tensor(seqlens)
+    st = vf.ScaleState().init()
+    ost = oscales.ScaleState()
+    if delayed:
+        st.set_ring_order(True)
+        ost.set_ring_order(True)
+    for p in range(16):
+        q, k, v = qkv(seqlens, H, D, 5000 + p, outliers=(p % 3 == 0))
+        vf.amax_update(st, q, k, v, cu)
+        oracle_push(ost, q, k, v)
+    state_matches(st.read(), ost)
+    ring_max = np.asarray(ost.hist, dtype=np.float32).max(axis=1)
+    for margin in (1.5, 1.0, 2.0, 1.25, 0.75):
+        static = vf.ScaleState().init()
+        saved = vf.calibrated_scales(st, margin, static)
+        torch.cuda.synchronize()
+        want = np.asarray(ocalib.saved_values(ring_max, margin), dtype=np.float32)
+        assert np.array_equal(saved.cpu().numpy().view(np.uint32), want.view(np.uint32)), margin
+        ref = oscales.ScaleState()
+        ref.set_static(*want.tolist())
+        state_matches(static.read(), ref)
+    assert st.device_error() == 0
+
+
+def test_device_calibrated_scales_empty_ring_is_an_error(vf):
+    """A state that saw no forward has no learned scale: the call records
+    VITFP8_ERR_INVALID_ARG in that state's error word and leaves the static
+    state as it was."""
+    st = vf.ScaleState().init()
+    static = vf.ScaleState().init().set_static(1.0, 2.0, 3.0)
+    before = static.read()
+    saved = vf.calibrated_scales(st, 1.5, static)
+    torch.cuda.synchronize()
+    assert st.device_error() == 1
+    assert static.read() == before
+    assert saved.cpu().tolist() == [0.0, 0.0, 0.0]
+    with pytest.raises(vf.VitFp8Error):
+        vf.calibrated_scales(st, float("nan"))
