@@ -780,6 +780,8 @@ def e2e(vf, run, stream, dev, steps, warmup, ws, pg):
     return {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
             "step_ms": [round(x, 2) for x in step_ms],
+            "median_ms_per_step": statistics.median(step_ms),
+            "value_at_median_step": ws * run.flops_layer * run.layers / (statistics.median(step_ms) * 1e-3) / 1e12,
             "link_gbs": {"h2d": h2d_link, "d2h": d2h_link,
                          "step_floor_ms": h2d / (h2d_link * 1e6)},
             "copies": "pinned host buffers; H2D, compute and D2H on three streams, overlapped across layers"}
