@@ -20,6 +20,8 @@
 //               issuers the waits of one overlap the other's MMAs.  The two
 //               streams write different accumulators, so their order in the
 //               tensor pipe does not matter.
+//   warp 11     idle (it completes the producer warpgroup of the register
+//               split below).
 //   warps 0-7   softmax: warp w owns the 16 rows 32(w%4) + 16(w/4) .. +15;
 //               two threads of the warp share each row (TMEM access shape
 //               16x32bx2), lanes 0-15 taking the keys 0..127 of a tile and
@@ -68,13 +70,35 @@
 
 namespace vitfp8 {
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same instruction): raise the calling warpgroup's per-thread register count
+// to N, or lower it to N and return the rest to the CTA's pool.
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 namespace fa {
 constexpr int BM = 128;                  // query rows per CTA
 constexpr int ROWS_PER_ITEM = BM;        // queries per work item
 constexpr int BN = 256;                  // keys per tile
 constexpr int HALF = BN / 2;             // keys per softmax thread and tile
 constexpr int NST = 3;                   // K/V pipeline stages
-constexpr int NUM_THREADS = 352;         // 8 softmax warps, TMA warp, S and P.V issuers
+constexpr int NUM_THREADS = 384;         // 8 softmax warps; TMA warp, S and P.V issuers, one idle warp
+// Registers: a launch of 384 threads gives every thread 168 (a scheduler hosts
+// three of the twelve warps).  Each warpgroup then moves to its own budget at
+// the top of its branch: the two softmax warpgroups up to REGS_SOFTMAX (a
+// 128-score half row, its 32 P words and the O rescale), the producer
+// warpgroup (TMA, the two issuers, an idle warp) down to REGS_PRODUCER.
+// 184 against the 160 a uniform budget allows: the compiler then schedules the
+// softmax loop with fewer stalls (1.6 % per tile on the 3xQHD layer).
+constexpr int REGS_SOFTMAX = 184;
+constexpr int REGS_PRODUCER = 120;
+static_assert(8 * 32 * REGS_SOFTMAX + 4 * 32 * REGS_PRODUCER <= NUM_THREADS * 168, "register split");
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;              // S issuer; owns the TMEM allocation
 constexpr int WARP_PV = 10;              // P.V issuer
@@ -186,128 +210,132 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEMPTR);
 
-    if (warp == WARP_TMA) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(BAR(B_QFULL), QBYTES);
-            tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, h, q0);
-            const uint32_t vbytes = 2u * uint32_t(p.DV) * 128u;
-            int j = 0;
-            for (; j < nkv; ++j) {
-                const int s = j % NST;
-                const int key0 = kbase + j * BN;
-                if (VF_CHECKED_BUILD && (key0 & 15) != 0) {
-                    // V^T copies start at token key0: TMA needs it 16-byte aligned.
-                    record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
-                    *abort_flag = 1;
-                    break;
+    if (warp >= 8) {
+        regs_decrease<REGS_PRODUCER>();
+        if (warp == WARP_TMA) {
+            // ------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+                mbar_arrive_expect_tx(BAR(B_QFULL), QBYTES);
+                tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, h, q0);
+                const uint32_t vbytes = 2u * uint32_t(p.DV) * 128u;
+                int j = 0;
+                for (; j < nkv; ++j) {
+                    const int s = j % NST;
+                    const int key0 = kbase + j * BN;
+                    if (VF_CHECKED_BUILD && (key0 & 15) != 0) {
+                        // V^T copies start at token key0: TMA needs it 16-byte aligned.
+                        record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    if (j >= NST && !bwait(BAR(B_KEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
+                    mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
+                    tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, key0);
+                    if (j >= NST && !bwait(BAR(B_VEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) {
+                        ++j;   // K_j is in flight: its barrier is drained below
+                        break;
+                    }
+                    mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
+                    tma_load_3d(sb + SM_V + s * VBYTES, &tmV, BAR(B_VFULL + s), key0, 0, h);
+                    tma_load_3d(sb + SM_V + s * VBYTES + VBLK, &tmV, BAR(B_VFULL + s), key0 + HALF, 0, h);
                 }
-                if (j >= NST && !bwait(BAR(B_KEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
-                mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
-                tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, key0);
-                if (j >= NST && !bwait(BAR(B_VEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) {
-                    ++j;   // K_j is in flight: its barrier is drained below
-                    break;
+                if (*abort_flag) {
+                    // Let the copies this thread started land before the CTA exits.
+                    bwait(BAR(B_QFULL), 0, abort_flag, err);
+                    for (int jj = (j > NST ? j - NST : 0); jj < j; ++jj) {
+                        const int s = jj % NST;
+                        const uint32_t ph = (jj / NST) & 1;
+                        for (int spin = 0; spin < (1 << 22); ++spin)
+                            if (mbar_try_wait(BAR(B_KFULL + s), ph)) break;
+                        for (int spin = 0; spin < (1 << 22); ++spin)
+                            if (mbar_try_wait(BAR(B_VFULL + s), ph)) break;
+                    }
                 }
-                mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
-                tma_load_3d(sb + SM_V + s * VBYTES, &tmV, BAR(B_VFULL + s), key0, 0, h);
-                tma_load_3d(sb + SM_V + s * VBYTES + VBLK, &tmV, BAR(B_VFULL + s), key0 + HALF, 0, h);
             }
-            if (*abort_flag) {
-                // Let the copies this thread started land before the CTA exits.
-                bwait(BAR(B_QFULL), 0, abort_flag, err);
-                for (int jj = (j > NST ? j - NST : 0); jj < j; ++jj) {
-                    const int s = jj % NST;
-                    const uint32_t ph = (jj / NST) & 1;
-                    for (int spin = 0; spin < (1 << 22); ++spin)
-                        if (mbar_try_wait(BAR(B_KFULL + s), ph)) break;
-                    for (int spin = 0; spin < (1 << 22); ++spin)
-                        if (mbar_try_wait(BAR(B_VFULL + s), ph)) break;
+        } else if (warp == WARP_MMA) {
+            // ------------------------------------------------ S issuer
+            if (lane == 0) {
+                const uint32_t idS = make_idesc(0, BM, BN);      // 128 x 256 per S product
+                // Descriptors are built once: within a 128-byte swizzled row a
+                // 32-byte K step adds 2 to the encoded start address; a stage
+                // adds its byte offset / 16.
+                const uint64_t dQ = sw128_kmajor_desc(sb + SM_Q);
+                const uint64_t dK0 = sw128_kmajor_desc(sb + SM_K);
+                const uint32_t tS = tmem + TM_S;
+                const int KS = p.KS;
+                auto issue_S = [&](int s) {
+                    const uint64_t dk = dK0 + uint64_t(s * (KBYTES >> 4));
+                    if (KS == 4) {
+                        umma_f8_ss_k4(tS, dQ, dk, idS, 0u);
+                    } else {
+                        umma_f8(tS, dQ, dk, idS, 0u);
+                        for (int kk = 1; kk < KS; ++kk)
+                            umma_f8(tS, dQ + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
+                    }
+                    tc_commit(BAR(B_SFULL));
+                    tc_commit(BAR(B_KEMPTY + s));
+                };
+                bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
+                          bwait(BAR(B_KFULL + 0), 0, abort_flag, err);
+                if (ok) {
+                    tc_fence_after();
+                    issue_S(0);
                 }
+                int s1 = 1 % NST;
+                uint32_t ph1 = NST == 1 ? 1u : 0u;
+                for (int j = 0; ok && j + 1 < nkv; ++j) {
+                    // S(j+1) as soon as K_{j+1} is in and every softmax warp has read S(j).
+                    if (!(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
+                    if (!(ok = bwait(BAR(B_SFREE), j & 1, abort_flag, err))) break;
+                    tc_fence_after();
+                    issue_S(s1);
+                    if (++s1 == NST) {
+                        s1 = 0;
+                        ph1 ^= 1u;
+                    }
+                }
+                // Every MMA issued above has completed before TMEM is released.
+                tc_commit(BAR(B_FINAL));
+                for (int spin = 0; spin < (1 << 24); ++spin)
+                    if (mbar_try_wait(BAR(B_FINAL), 0)) break;
+            }
+        } else if (warp == WARP_PV) {
+            // ------------------------------------------------ P.V issuer
+            if (lane == 0) {
+                const uint32_t idPV = make_idesc(0, BM, p.DV + 16);   // d columns + the l column block
+                const uint64_t dV0 = sw128_kmajor_desc(sb + SM_V);
+                const uint32_t tO = tmem + TM_O, tP = tmem + TM_P;
+                int s = 0;
+                uint32_t ph = 0;
+                bool ok = true;
+                for (int j = 0; ok && j < nkv; ++j) {
+                    // O += P(j) V_j: 256 keys in 8 steps of 32, keys 0..127 from
+                    // V^T block 0 and P columns 0..31, keys 128..255 from block 1
+                    // and P columns 32..63.
+                    if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
+                    if (!(ok = bwait(BAR(B_PFULL), j & 1, abort_flag, err))) break;
+                    tc_fence_after();
+                    const uint64_t dv = dV0 + uint64_t(s * (VBYTES >> 4));
+                    umma_f8_ts_k4(tO, tP, dv, idPV, j > 0 ? 1u : 0u);
+                    umma_f8_ts_k4(tO, tP + 32u, dv + uint64_t(VBLK >> 4), idPV, 1u);
+                    tc_commit(BAR(B_OFULL));
+                    tc_commit(BAR(B_VEMPTY + s));
+                    if (++s == NST) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                tc_commit(BAR(B_FINAL));
+                for (int spin = 0; spin < (1 << 24); ++spin)
+                    if (mbar_try_wait(BAR(B_FINAL), 0)) break;
             }
         }
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------ S issuer
-        if (lane == 0) {
-            const uint32_t idS = make_idesc(0, BM, BN);      // 128 x 256 per S product
-            // Descriptors are built once: within a 128-byte swizzled row a
-            // 32-byte K step adds 2 to the encoded start address; a stage
-            // adds its byte offset / 16.
-            const uint64_t dQ = sw128_kmajor_desc(sb + SM_Q);
-            const uint64_t dK0 = sw128_kmajor_desc(sb + SM_K);
-            const uint32_t tS = tmem + TM_S;
-            const int KS = p.KS;
-            auto issue_S = [&](int s) {
-                const uint64_t dk = dK0 + uint64_t(s * (KBYTES >> 4));
-                if (KS == 4) {
-                    umma_f8_ss_k4(tS, dQ, dk, idS, 0u);
-                } else {
-                    umma_f8(tS, dQ, dk, idS, 0u);
-                    for (int kk = 1; kk < KS; ++kk)
-                        umma_f8(tS, dQ + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
-                }
-                tc_commit(BAR(B_SFULL));
-                tc_commit(BAR(B_KEMPTY + s));
-            };
-            bool ok = bwait(BAR(B_QFULL), 0, abort_flag, err) &&
-                      bwait(BAR(B_KFULL + 0), 0, abort_flag, err);
-            if (ok) {
-                tc_fence_after();
-                issue_S(0);
-            }
-            int s1 = 1 % NST;
-            uint32_t ph1 = NST == 1 ? 1u : 0u;
-            for (int j = 0; ok && j + 1 < nkv; ++j) {
-                // S(j+1) as soon as K_{j+1} is in and every softmax warp has read S(j).
-                if (!(ok = bwait(BAR(B_KFULL + s1), ph1, abort_flag, err))) break;
-                if (!(ok = bwait(BAR(B_SFREE), j & 1, abort_flag, err))) break;
-                tc_fence_after();
-                issue_S(s1);
-                if (++s1 == NST) {
-                    s1 = 0;
-                    ph1 ^= 1u;
-                }
-            }
-            // Every MMA issued above has completed before TMEM is released.
-            tc_commit(BAR(B_FINAL));
-            for (int spin = 0; spin < (1 << 24); ++spin)
-                if (mbar_try_wait(BAR(B_FINAL), 0)) break;
-        }
-    } else if (warp == WARP_PV) {
-        // ------------------------------------------------ P.V issuer
-        if (lane == 0) {
-            const uint32_t idPV = make_idesc(0, BM, p.DV + 16);   // d columns + the l column block
-            const uint64_t dV0 = sw128_kmajor_desc(sb + SM_V);
-            const uint32_t tO = tmem + TM_O, tP = tmem + TM_P;
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int j = 0; ok && j < nkv; ++j) {
-                // O += P(j) V_j: 256 keys in 8 steps of 32, keys 0..127 from
-                // V^T block 0 and P columns 0..31, keys 128..255 from block 1
-                // and P columns 32..63.
-                if (!(ok = bwait(BAR(B_VFULL + s), ph, abort_flag, err))) break;
-                if (!(ok = bwait(BAR(B_PFULL), j & 1, abort_flag, err))) break;
-                tc_fence_after();
-                const uint64_t dv = dV0 + uint64_t(s * (VBYTES >> 4));
-                umma_f8_ts_k4(tO, tP, dv, idPV, j > 0 ? 1u : 0u);
-                umma_f8_ts_k4(tO, tP + 32u, dv + uint64_t(VBLK >> 4), idPV, 1u);
-                tc_commit(BAR(B_OFULL));
-                tc_commit(BAR(B_VEMPTY + s));
-                if (++s == NST) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-            tc_commit(BAR(B_FINAL));
-            for (int spin = 0; spin < (1 << 24); ++spin)
-                if (mbar_try_wait(BAR(B_FINAL), 0)) break;
-        }
-    } else if (warp < 8) {
+    } else {
         // ------------------------------------------------ softmax (warps 0..7)
+        regs_increase<REGS_SOFTMAX>();
         const int half = lane >> 4;           // keys half*128 .. half*128+127 of each tile
         const int rbase = 32 * (warp & 3) + 16 * (warp >> 2);
         const int r = rbase + (lane & 15);    // row inside the query tile
