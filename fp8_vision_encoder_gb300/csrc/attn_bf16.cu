@@ -78,23 +78,13 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                  const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using namespace fb;
     const int item = blockIdx.x;
-    const int total = p.ws->total_items;
-    if (item >= total) return;
-
-    int lo = 0, hi = p.nseq - 1;  // largest pos with prefix[pos] <= item
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (!VF_IN(mid, 1, p.nseq + 1, &p.ws->error)) return;
-        if (p.prefix[mid] <= item) lo = mid; else hi = mid - 1;
-    }
-    if (!VF_IN(lo, 1, p.nseq, &p.ws->error)) return;
-    const int b = p.order[lo];
-    if (!VF_IN(b, 2, p.nseq + 1, &p.ws->error)) return;
-    const int local = item - p.prefix[lo];
-    const int seg_s = p.cu[b];
-    const int seg_e = p.cu[b + 1];
-    const int L = seg_e - seg_s;
-    const int nq = (L + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
+    SegRec rec;
+    int total;
+    if (!find_item(p, item, rec, total) || item >= total) return;
+    const int local = item - rec.first_item;
+    const int seg_s = rec.seg_s;
+    const int seg_e = rec.seg_e;
+    const int nq = rec.nq;
     const int h = local / nq;
     const int qt = local - h * nq;
     const int q0 = seg_s + qt * ROWS_PER_ITEM;
@@ -460,8 +450,7 @@ vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint1
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     AttnParams prm;
     prm.cu = cu;
-    prm.order = reinterpret_cast<const int32_t*>(hdr + 1);
-    prm.prefix = prm.order + nseq;
+    prm.rec = reinterpret_cast<const SegRec*>(hdr + 1);
     prm.ws = hdr;
     prm.st = nullptr;
     prm.out = out;

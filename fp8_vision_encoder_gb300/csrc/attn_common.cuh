@@ -14,8 +14,7 @@ constexpr long long ATTN_WAIT_LIMIT = 1000000000LL;  // cycles (~0.5 s) before a
 
 struct AttnParams {
     const int32_t* cu;
-    const int32_t* order;
-    const int32_t* prefix;
+    const SegRec* rec;      // work-list records, longest segment first
     WsHeader* ws;
     const vitfp8_scale_state* st;
     uint16_t* out;
@@ -23,6 +22,42 @@ struct AttnParams {
     float sm_scale;
     int64_t out_elems;  // T * H * D (checked build)
 };
+
+// Work item -> the record of its segment (the last record whose first_item
+// is <= item) and the call's item count.  Every lane of the calling warp must
+// call it: with at most 32 records each lane loads one and a vote picks it
+// (one round trip to memory); otherwise a binary search over the records.
+// False (checked build) if an index falls outside the work list.
+__device__ __forceinline__ bool find_item(const AttnParams& p, int item, SegRec& r, int& total) {
+    const int lane = threadIdx.x & 31;
+    total = p.ws->total_items;
+    if (p.nseq <= 32) {
+        int4 mine = make_int4(0x7FFFFFFF, 0, 0, 0);
+        if (lane < p.nseq && VF_IN(lane, 1, p.nseq, &p.ws->error))
+            mine = *reinterpret_cast<const int4*>(p.rec + lane);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, lane < p.nseq && mine.x <= item);
+        if (m == 0u) return false;   // only when item is past every record (no work)
+        const int lo = 31 - __clz(m);
+        r.first_item = __shfl_sync(0xFFFFFFFFu, mine.x, lo);
+        r.seg_s = __shfl_sync(0xFFFFFFFFu, mine.y, lo);
+        r.seg_e = __shfl_sync(0xFFFFFFFFu, mine.z, lo);
+        r.nq = __shfl_sync(0xFFFFFFFFu, mine.w, lo);
+        return true;
+    }
+    int lo = 0, hi = p.nseq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (!VF_IN(mid, 1, p.nseq, &p.ws->error)) return false;
+        if (p.rec[mid].first_item <= item) lo = mid; else hi = mid - 1;
+    }
+    if (!VF_IN(lo, 1, p.nseq, &p.ws->error)) return false;
+    const int4 v = *reinterpret_cast<const int4*>(p.rec + lo);
+    r.first_item = v.x;
+    r.seg_s = v.y;
+    r.seg_e = v.z;
+    r.nq = v.w;
+    return true;
+}
 
 // Bounded wait: true when the phase with `parity` completed; false if the CTA
 // aborted or this wait timed out (which sets the abort flag and the error).

@@ -10,7 +10,9 @@
 //
 //   warp 8      TMA producer: the Q tile once, then K tiles (256 keys x 128 d)
 //               and V^T tiles (d x 256 keys) through a shared-memory ring
-//               (128-byte swizzle).
+//               (128-byte swizzle).  Its lane 0 also initialises the barriers
+//               and starts the Q tile and the first ring's tiles before the
+//               CTA-wide set-up sync, so those copies overlap the set-up.
 //   warp 9      S issuer (one thread), tcgen05.mma kind::f8f6f4 (E4M3 x E4M3
 //               -> F32) into tensor memory: S(j+1) = Q K_{j+1}^T (N = 256) as
 //               soon as the softmax has read S(j).
@@ -82,6 +84,17 @@ __device__ __forceinline__ void regs_decrease() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Named CTA barrier `ID` over `COUNT` threads: arrive without waiting, or
+// arrive and wait for all COUNT.
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_bar_arrive() {
+    asm volatile("bar.arrive %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_bar_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+
 namespace fa {
 constexpr int BM = 128;                  // query rows per CTA
 constexpr int ROWS_PER_ITEM = BM;        // queries per work item
@@ -140,24 +153,14 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using namespace fa;
     const int item = blockIdx.x;
-    const int total = p.ws->total_items;
-    if (item >= total) return;
-
-    // ---- work item -> (segment, head, query tile)
-    int lo = 0, hi = p.nseq - 1;  // largest pos with prefix[pos] <= item
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (!VF_IN(mid, 1, p.nseq + 1, &p.ws->error)) return;
-        if (p.prefix[mid] <= item) lo = mid; else hi = mid - 1;
-    }
-    if (!VF_IN(lo, 1, p.nseq, &p.ws->error)) return;
-    const int b = p.order[lo];
-    if (!VF_IN(b, 2, p.nseq + 1, &p.ws->error)) return;
-    const int local = item - p.prefix[lo];
-    const int seg_s = p.cu[b];
-    const int seg_e = p.cu[b + 1];
-    const int L = seg_e - seg_s;
-    const int nq = (L + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
+    // ---- work item -> (segment, head, query tile): one record of the work list
+    SegRec rec;
+    int total;
+    if (!find_item(p, item, rec, total) || item >= total) return;
+    const int local = item - rec.first_item;
+    const int seg_s = rec.seg_s;
+    const int seg_e = rec.seg_e;
+    const int nq = rec.nq;
     const int h = local / nq;
     const int qt = local - h * nq;
     const int q0 = seg_s + qt * ROWS_PER_ITEM;
@@ -175,17 +178,25 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Rows DV..DV+15 of every V^T block hold E4M3 1.0 (0x38) for good: the
-    // TMA boxes cover rows 0..DV-1 only.  (Uniform bytes: the swizzle does not
-    // matter.)  The tensor core reads them through the async proxy.
-    for (int i = threadIdx.x; i < NST * 2 * 16 * 32; i += blockDim.x) {
-        const int blk = i / (16 * 32);
-        const int w = i - blk * (16 * 32);
-        if (VF_IN(blk * VBLK + p.DV * 128 + 4 * w, 4, NST * VBYTES, &p.ws->error))
-            reinterpret_cast<uint32_t*>(smem + SM_V + blk * VBLK + p.DV * 128)[w] = 0x38383838u;
-    }
-    fence_proxy_async_smem();
-    if (threadIdx.x == 0) {
+    // The TMA thread initialises the barriers and starts the copies the first
+    // S product needs (the Q tile and K tile 0) at once, so they are in flight
+    // while the CTA sets up the ones rows and TMEM; the rest of the first ring
+    // follows right after the CTA-wide sync (no other thread touches a
+    // barrier before it).
+    const uint32_t vbytes = 2u * uint32_t(p.DV) * 128u;
+    auto load_k = [&](int j) {
+        const int s = j % NST;
+        mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
+        tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, kbase + j * BN);
+    };
+    auto load_v = [&](int j) {
+        const int s = j % NST;
+        const int key0 = kbase + j * BN;
+        mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
+        tma_load_3d(sb + SM_V + s * VBYTES, &tmV, BAR(B_VFULL + s), key0, 0, h);
+        tma_load_3d(sb + SM_V + s * VBYTES + VBLK, &tmV, BAR(B_VFULL + s), key0 + HALF, 0, h);
+    };
+    if (warp == WARP_TMA && lane == 0) {
         mbar_init(BAR(B_QFULL), 1);
         for (int s = 0; s < NST; ++s) {
             mbar_init(BAR(B_KFULL + s), 1);
@@ -200,52 +211,81 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(BAR(B_FINAL), 2);   // one commit per issuer
         *abort_flag = 0;
         fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_arrive_expect_tx(BAR(B_QFULL), QBYTES);
+        tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, h, q0);
+        // V^T copies start at token kbase + j * BN, a multiple of 16: TMA needs
+        // the innermost coordinate 16-byte aligned (checked in the checked build).
+        if (VF_CHECKED_BUILD && (kbase & 15) != 0) {
+            record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
+            *abort_flag = 1;
+        } else {
+            load_k(0);
+        }
     }
-    if (warp == WARP_MMA) {
-        tmem_alloc(sb + SM_TMEMPTR, TMEM_COLS);
-        tmem_relinquish();
+
+    // Set-up sync on named barrier 1: the TMA warp only arrives (once the
+    // barriers are initialised) and goes straight on with its copies; every
+    // other warp also writes the ones rows and allocates TMEM, then waits.
+    uint32_t tmem = 0;
+    if (warp == WARP_TMA) {
+        __syncwarp();
+        __threadfence_block();
+        named_bar_arrive<1, NUM_THREADS>();
+    } else {
+        // Rows DV..DV+15 of every V^T block hold E4M3 1.0 (0x38) for good:
+        // the TMA boxes cover rows 0..DV-1 only.  (Uniform bytes: the swizzle
+        // does not matter.)  The tensor core reads them through the async
+        // proxy.
+        const int t = threadIdx.x < 32 * WARP_TMA ? threadIdx.x : threadIdx.x - 32;
+        for (int i = t; i < NST * 2 * 16 * 32; i += NUM_THREADS - 32) {
+            const int blk = i / (16 * 32);
+            const int w = i - blk * (16 * 32);
+            if (VF_IN(blk * VBLK + p.DV * 128 + 4 * w, 4, NST * VBYTES, &p.ws->error))
+                reinterpret_cast<uint32_t*>(smem + SM_V + blk * VBLK + p.DV * 128)[w] = 0x38383838u;
+        }
+        fence_proxy_async_smem();
+        if (warp == WARP_MMA) {
+            tmem_alloc(sb + SM_TMEMPTR, TMEM_COLS);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        named_bar_sync<1, NUM_THREADS>();
+        tc_fence_after();
+        tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEMPTR);
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEMPTR);
 
     if (warp >= 8) {
         regs_decrease<REGS_PRODUCER>();
         if (warp == WARP_TMA) {
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
-                tma_prefetch_desc(&tmQ);
-                tma_prefetch_desc(&tmK);
-                tma_prefetch_desc(&tmV);
-                mbar_arrive_expect_tx(BAR(B_QFULL), QBYTES);
-                tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, h, q0);
-                const uint32_t vbytes = 2u * uint32_t(p.DV) * 128u;
-                int j = 0;
-                for (; j < nkv; ++j) {
-                    const int s = j % NST;
-                    const int key0 = kbase + j * BN;
-                    if (VF_CHECKED_BUILD && (key0 & 15) != 0) {
-                        // V^T copies start at token key0: TMA needs it 16-byte aligned.
-                        record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
-                        *abort_flag = 1;
-                        break;
+                // The Q tile and K tile 0 are in flight since the set-up
+                // (neither K nor V if the set-up found kbase misaligned): V
+                // tile 0 and K/V tiles 1..NST-1 go at once, while the other
+                // warps finish their set-up; tile j >= NST reuses its stage
+                // once S and P.V of tile j - NST are done with it.
+                int issued = 0;   // K/V tiles whose copies were started
+                if (!*abort_flag) {
+                    load_v(0);
+                    issued = 1;
+                    for (int j = 1; j < nkv; ++j) {
+                        const int s = j % NST;
+                        if (j >= NST && !bwait(BAR(B_KEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
+                        if (j >= NST && !bwait(BAR(B_VEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
+                        load_k(j);
+                        load_v(j);
+                        issued = j + 1;
                     }
-                    if (j >= NST && !bwait(BAR(B_KEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) break;
-                    mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
-                    tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, key0);
-                    if (j >= NST && !bwait(BAR(B_VEMPTY + s), ((j / NST) - 1) & 1, abort_flag, err)) {
-                        ++j;   // K_j is in flight: its barrier is drained below
-                        break;
-                    }
-                    mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
-                    tma_load_3d(sb + SM_V + s * VBYTES, &tmV, BAR(B_VFULL + s), key0, 0, h);
-                    tma_load_3d(sb + SM_V + s * VBYTES + VBLK, &tmV, BAR(B_VFULL + s), key0 + HALF, 0, h);
                 }
                 if (*abort_flag) {
-                    // Let the copies this thread started land before the CTA exits.
-                    bwait(BAR(B_QFULL), 0, abort_flag, err);
-                    for (int jj = (j > NST ? j - NST : 0); jj < j; ++jj) {
+                    // Let the copies this thread started land before the CTA
+                    // exits (bounded spins; these barriers were armed).
+                    for (int spin = 0; spin < (1 << 22); ++spin)
+                        if (mbar_try_wait(BAR(B_QFULL), 0)) break;
+                    for (int jj = (issued > NST ? issued - NST : 0); jj < issued; ++jj) {
                         const int s = jj % NST;
                         const uint32_t ph = (jj / NST) & 1;
                         for (int spin = 0; spin < (1 << 22); ++spin)
@@ -347,6 +387,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t tP = tmem + lane_off + TM_P;
         const float c = p.st->scale[0] * p.st->scale[1] * p.sm_scale * 1.4426950408889634f;
         const uint64_t c2 = f32x2_pack(c, c);
+        const float scale_v = p.st->scale[2];   // read now: the epilogue needs it last
         float m_ref = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
@@ -456,7 +497,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             uint32_t lbits;   // both halves: a copy of l (column DV)
             uint32_t oa[32], ob[32], oc[16];
             tmem_ld_o80<OSPLIT>(tO, tO + uint32_t(p.DV), oa, ob, oc, lbits);
-            const float oscale = p.st->scale[2] / __uint_as_float(lbits);
+            const float oscale = scale_v / __uint_as_float(lbits);
             uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
             const int cbase = half * OSPLIT;
             auto store8 = [&](int d0, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
@@ -490,14 +531,19 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
-// Work list: segments sorted longest first (when there are at most 2048),
-// items per segment = ceil(L / rows_per_item) * H, prefix sums over the sorted order.
+// Work list: one record per segment, segments sorted longest first (when
+// there are at most 2048; in cu_seqlens order otherwise), items per segment =
+// ceil(L / rows_per_item) * H, each record's first_item the items of all
+// records before it (a block-wide scan, 1024 records per step).
 __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T, int H,
-                                 int rows_per_item, WsHeader* ws, int32_t* order, int32_t* prefix) {
+                                 int rows_per_item, WsHeader* ws, SegRec* rec) {
     __shared__ int bad;
+    __shared__ int warp_sum[32];
+    __shared__ int carry;
     if (threadIdx.x == 0) {
         ws->error = 0;
         bad = (cu[0] != 0 || cu[nseq] != T) ? 1 : 0;
+        carry = 0;
     }
     __syncthreads();
     for (int b = threadIdx.x; b < nseq; b += blockDim.x)
@@ -521,20 +567,42 @@ __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T
                 rank += (L2 > Lb) || (L2 == Lb && b2 < b);
             }
         }
-        if (VF_IN(rank, 1, nseq, &ws->error)) order[rank] = b;
+        if (VF_IN(rank, 1, nseq, &ws->error))
+            *reinterpret_cast<int4*>(rec + rank) =
+                make_int4(0, cu[b], cu[b + 1], (Lb + rows_per_item - 1) / rows_per_item);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        prefix[0] = 0;
-        for (int i = 0; i < nseq; ++i) {
-            const int bb = order[i];
-            if (!VF_IN(bb, 2, nseq + 1, &ws->error)) break;
-            const int Lb = cu[bb + 1] - cu[bb];
-            acc += ((Lb + rows_per_item - 1) / rows_per_item) * H;
-            prefix[i + 1] = acc;
+    // first_item: exclusive scan of nq * H over the records, 1024 at a time.
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int base = 0; base < nseq; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const int v = i < nseq ? rec[i].nq * H : 0;
+        int x = v;   // inclusive warp scan
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
         }
-        ws->total_items = acc;
+        if (lane == 31) warp_sum[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int w = lane < nw ? warp_sum[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+                if (lane >= o) w += y;
+            }
+            if (lane < nw) warp_sum[lane] = w;   // inclusive prefix of warp totals
+        }
+        __syncthreads();
+        const int before = carry + (wid > 0 ? warp_sum[wid - 1] : 0) + x - v;
+        if (i < nseq) rec[i].first_item = before;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = before + v;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        ws->total_items = carry;
         ws->num_seqs = nseq;
     }
 }
@@ -582,9 +650,8 @@ PerDeviceOnce g_smem_attr;
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
                              void* ws, cudaStream_t s) {
     WsHeader* hdr = static_cast<WsHeader*>(ws);
-    int32_t* order = reinterpret_cast<int32_t*>(hdr + 1);
-    int32_t* prefix = order + nseq;
-    attn_plan_kernel<<<1, 1024, 0, s>>>(cu, nseq, T, H, rows_per_item, hdr, order, prefix);
+    attn_plan_kernel<<<1, 1024, 0, s>>>(cu, nseq, T, H, rows_per_item, hdr,
+                                        reinterpret_cast<SegRec*>(hdr + 1));
     return cudaGetLastError();
 }
 
@@ -615,8 +682,7 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     AttnParams prm;
     prm.cu = cu;
-    prm.order = reinterpret_cast<const int32_t*>(hdr + 1);
-    prm.prefix = prm.order + nseq;
+    prm.rec = reinterpret_cast<const SegRec*>(hdr + 1);
     prm.ws = hdr;
     prm.st = st;
     prm.out = out;

@@ -17,8 +17,9 @@ struct SrcDev {
     int64_t extent;  // elements the layout addresses (checked build)
 };
 
-// Attention workspace header (device), followed by int32 order[num_seqs] and
-// int32 prefix[num_seqs + 1].
+// Attention workspace: a header, then one record per segment in the work
+// list's order (longest first), so that a CTA finds its segment with one
+// 16-byte load per probe.
 struct WsHeader {
     int32_t error;        // first device-detected vitfp8_status
     int32_t total_items;  // work items of the current call
@@ -27,8 +28,15 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 
+struct SegRec {
+    int32_t first_item;   // work items of all earlier records
+    int32_t seg_s, seg_e; // the segment's packed token range
+    int32_t nq;           // its query tiles (items per head)
+};
+static_assert(sizeof(SegRec) == 16, "one 16-byte load per record");
+
 inline size_t ws_bytes(int32_t num_seqs) {
-    size_t b = sizeof(WsHeader) + sizeof(int32_t) * (2 * size_t(num_seqs) + 1);
+    size_t b = sizeof(WsHeader) + sizeof(SegRec) * size_t(num_seqs);
     return (b + 255) & ~size_t(255);
 }
 

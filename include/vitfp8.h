@@ -301,7 +301,7 @@ vitfp8_status vitfp8_attn_varlen_bf16(const vitfp8_bf16* q, const vitfp8_bf16* k
  *
  * Arguments, layouts and the computation are exactly those of
  * vitfp8_attn_varlen.  The work list lives instead in a fixed device array
- * inside the library (about 33 KB; every GPU that loads the library keeps it
+ * inside the library (about 64 KB; every GPU that loads the library keeps it
  * until the process exits), sized for at most VITFP8_NOALLOC_MAX_SEQS
  * segments: num_seqs above that returns VITFP8_ERR_UNSUPPORTED without
  * launching.  The first call on each device looks up that array's device
