@@ -439,7 +439,7 @@ vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint1
     if (!make_map_bf16(&mq, q, T, H, D) || !make_map_bf16(&mk, k, T, H, D) ||
         !make_map_bf16(&mv, v, T, H, D))
         return VITFP8_ERR_CUDA;
-    if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, ws, s) != cudaSuccess) return VITFP8_ERR_CUDA;
+    if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, 0, 0, ws, s) != cudaSuccess) return VITFP8_ERR_CUDA;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return VITFP8_ERR_CUDA;
     if (!g_smem_attr_b.run(dev, [] {
@@ -454,6 +454,8 @@ vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint1
     prm.ws = hdr;
     prm.st = nullptr;
     prm.out = out;
+    prm.split_cnt = nullptr;   // no key-range split in this kernel
+    prm.split_part = nullptr;
     prm.nseq = nseq;
     prm.T = T;
     prm.H = H;

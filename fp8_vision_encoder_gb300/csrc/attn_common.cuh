@@ -18,23 +18,31 @@ struct AttnParams {
     WsHeader* ws;
     const vitfp8_scale_state* st;
     uint16_t* out;
+    int32_t* split_cnt;     // per split work item: parts finished (zeroed by the plan)
+    float* split_part;      // per split part: kSplitPartBytes of partial results
     int nseq, T, H, D, Dp, DV, KS;
     float sm_scale;
     int64_t out_elems;  // T * H * D (checked build)
 };
 
 // Work item -> the record of its segment (the last record whose first_item
-// is <= item) and the call's item count.  Every lane of the calling warp must
-// call it: with at most 32 records each lane loads one and a vote picks it
-// (one round trip to memory); otherwise a binary search over the records.
-// False (checked build) if an index falls outside the work list.
-__device__ __forceinline__ bool find_item(const AttnParams& p, int item, SegRec& r, int& total) {
+// is <= item).  In two steps so that a caller can issue every load it needs
+// before it knows the item: find_item_load reads, with at most 32 records,
+// the calling lane's record (every lane of the warp must call both steps);
+// find_item_pick then picks the record by a vote, or else binary-searches the
+// records.  False (checked build) if an index falls outside the work list,
+// or if item is past every record.
+__device__ __forceinline__ int4 find_item_load(const AttnParams& p) {
     const int lane = threadIdx.x & 31;
-    total = p.ws->total_items;
+    int4 mine = make_int4(0x7FFFFFFF, 0, 0, 0);
+    if (p.nseq <= 32 && lane < p.nseq && VF_IN(lane, 1, p.nseq, &p.ws->error))
+        mine = *reinterpret_cast<const int4*>(p.rec + lane);
+    return mine;
+}
+
+__device__ __forceinline__ bool find_item_pick(const AttnParams& p, int item, int4 mine, SegRec& r) {
+    const int lane = threadIdx.x & 31;
     if (p.nseq <= 32) {
-        int4 mine = make_int4(0x7FFFFFFF, 0, 0, 0);
-        if (lane < p.nseq && VF_IN(lane, 1, p.nseq, &p.ws->error))
-            mine = *reinterpret_cast<const int4*>(p.rec + lane);
         const unsigned m = __ballot_sync(0xFFFFFFFFu, lane < p.nseq && mine.x <= item);
         if (m == 0u) return false;   // only when item is past every record (no work)
         const int lo = 31 - __clz(m);
@@ -57,6 +65,12 @@ __device__ __forceinline__ bool find_item(const AttnParams& p, int item, SegRec&
     r.seg_e = v.z;
     r.nq = v.w;
     return true;
+}
+
+// Both steps, and the call's item count.
+__device__ __forceinline__ bool find_item(const AttnParams& p, int item, SegRec& r, int& total) {
+    total = p.ws->total_items;
+    return find_item_pick(p, item, find_item_load(p), r);
 }
 
 // Bounded wait: true when the phase with `parity` completed; false if the CTA

@@ -57,6 +57,13 @@
 // V^T tile starts at a 16-byte-aligned token coordinate; keys outside the
 // segment are masked to -inf (only the first and last tile need it).
 //
+// Key-range split of the last wave: when the work items leave a last wave
+// that would keep at most half the SMs busy for a whole item, the plan cuts
+// each item of that wave into up to four parts of consecutive key tiles (one
+// CTA each).  A part runs the same pipeline over its tiles, stores O, l and
+// its reference in the workspace, and the part that finishes last combines
+// the parts by exact powers of two and writes the rows.
+//
 // Every wait (mbarrier or shared-memory handshake) is bounded; on expiry the
 // CTA records VITFP8_ERR_DEVICE_TIMEOUT in the workspace error word, all roles
 // leave their loops, wait (bounded) for their own async work, free TMEM and
@@ -107,10 +114,11 @@ constexpr int NUM_THREADS = 384;         // 8 softmax warps; TMA warp, S and P.V
 // the top of its branch: the two softmax warpgroups up to REGS_SOFTMAX (a
 // 128-score half row, its 32 P words and the O rescale), the producer
 // warpgroup (TMA, the two issuers, an idle warp) down to REGS_PRODUCER.
-// 184 against the 160 a uniform budget allows: the compiler then schedules the
-// softmax loop with fewer stalls (1.6 % per tile on the 3xQHD layer).
-constexpr int REGS_SOFTMAX = 184;
-constexpr int REGS_PRODUCER = 120;
+// 176 against the 160 a uniform budget allows: the compiler then schedules the
+// softmax loop with fewer stalls (about 1.5 % per tile on the 3xQHD layer);
+// 152 keeps the producer warpgroup free of spills.
+constexpr int REGS_SOFTMAX = 176;
+constexpr int REGS_PRODUCER = 152;
 static_assert(8 * 32 * REGS_SOFTMAX + 4 * 32 * REGS_PRODUCER <= NUM_THREADS * 168, "register split");
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;              // S issuer; owns the TMEM allocation
@@ -140,23 +148,172 @@ constexpr int B_FINAL = B_OFULL + 1;
 constexpr int NBAR = B_FINAL + 1;
 constexpr int SM_TMEMPTR = SM_BAR + NBAR * 8;
 constexpr int SM_ABORT = SM_TMEMPTR + 4;
-constexpr int SM_USED = SM_ABORT + 4;
+constexpr int SM_LAST = SM_ABORT + 4;      // key-range split: this CTA merges the parts
+constexpr int SM_SPLIT = SM_LAST + 4;      // key-range split: slot, item index, parts (3 ints)
+constexpr int SM_USED = SM_SPLIT + 12;
 constexpr int SMEM_BYTES = SM_USED + 1024;  // + slack to align the base to 1024
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 448;
 constexpr int OSPLIT = 80;               // O columns per half-row thread (2 x 80 >= 128 + 16)
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// A split part's partial results: per softmax thread its OSPLIT O columns
+// (OSPLIT / 4 chunks of four floats, chunk-major so a warp's stores coalesce),
+// then (l, m_ref) per thread.
+constexpr int PART_CHUNKS = OSPLIT / 4;
+constexpr int PART_LM = PART_CHUNKS * 256 * 4;   // float offset of the (l, m_ref) pairs
+constexpr int PART_FLOATS = PART_LM + 2 * 256;
+static_assert(PART_FLOATS * sizeof(float) <= kSplitPartBytes, "split part fits its slot");
 }  // namespace fa
+
+// Epilogue of one part of a split work item (softmax threads 0..255, called
+// by all of them): slot = its part's index among the split CTAs, grp = its
+// item's index among the split items, sp_k = parts per item.  O, l and the reference cover this part's key tiles only.
+// Every part stores them in its workspace slot (output columns < D only); the
+// part that arrives last combines all parts in part order, so the result does
+// not depend on which part that is:
+//   M = max_p m_p,  O = sum_p O_p 2^(m_p - M),  l = sum_p l_p 2^(m_p - M),
+// exact powers of two as in the single-pass rescale.  Kept out of line so
+// that it does not take registers from the tile loop.
+struct SplitOut {
+    float* part;          // the workspace's partial-result slots
+    int32_t* cnt;         // per split item: parts finished
+    uint16_t* out;        // bf16 output row of this thread's query (h included)
+    int32_t* err;
+    int64_t out_off;      // that row's first element index (checked build)
+    int64_t out_elems;
+    int D, DV;
+};
+
+__device__ __noinline__ void split_part_epilogue(const SplitOut so, uint32_t tO, bool row_valid, int half,
+                                                 float m_ref, float scale_v, int slot, int grp, int sp_k,
+                                                 bool ok, volatile int* abort_flag, uint8_t* last_flag) {
+    using namespace fa;
+    int32_t* err = so.err;
+    const int tid = threadIdx.x;   // 0..255: the softmax threads
+    const int cbase = half * OSPLIT;
+    constexpr size_t PSTRIDE = kSplitPartBytes / sizeof(float);
+    if (!VF_IN(slot, 1, kSplitMaxParts, err)) ok = false;
+    if (ok) {
+        tc_fence_after();
+        uint32_t lbits;
+        uint32_t oa[32], ob[32], oc[16];
+        tmem_ld_o80<OSPLIT>(tO, tO + uint32_t(so.DV), oa, ob, oc, lbits);
+        float* mine = so.part + size_t(slot) * PSTRIDE;
+        uint4* dst = reinterpret_cast<uint4*>(mine);
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) {
+            if (cbase + 4 * q + 8 <= so.D) {
+                __stcg(dst + q * 256 + tid, make_uint4(oa[4 * q], oa[4 * q + 1], oa[4 * q + 2], oa[4 * q + 3]));
+                __stcg(dst + (q + 1) * 256 + tid,
+                       make_uint4(oa[4 * q + 4], oa[4 * q + 5], oa[4 * q + 6], oa[4 * q + 7]));
+            }
+            if (cbase + 32 + 4 * q + 8 <= so.D) {
+                __stcg(dst + (8 + q) * 256 + tid, make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]));
+                __stcg(dst + (9 + q) * 256 + tid,
+                       make_uint4(ob[4 * q + 4], ob[4 * q + 5], ob[4 * q + 6], ob[4 * q + 7]));
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; q += 2) {
+            if (cbase + 64 + 4 * q + 8 <= so.D) {
+                __stcg(dst + (16 + q) * 256 + tid,
+                       make_uint4(oc[4 * q], oc[4 * q + 1], oc[4 * q + 2], oc[4 * q + 3]));
+                __stcg(dst + (17 + q) * 256 + tid,
+                       make_uint4(oc[4 * q + 4], oc[4 * q + 5], oc[4 * q + 6], oc[4 * q + 7]));
+            }
+        }
+        __stcg(reinterpret_cast<float2*>(mine + PART_LM) + tid, make_float2(__uint_as_float(lbits), m_ref));
+    }
+    __threadfence();
+    named_bar_sync<2, 256>();
+    if (tid == 0) {
+        int last = 0;
+        if (!*abort_flag && VF_IN(grp, 1, kSplitMaxParts, err))
+            last = atomicAdd(so.cnt + grp, 1) == sp_k - 1;
+        *reinterpret_cast<volatile int*>(last_flag) = last;
+    }
+    named_bar_sync<2, 256>();
+    if (!ok || !*reinterpret_cast<volatile int*>(last_flag)) return;
+    __threadfence();
+    const float* base = so.part + size_t(grp) * sp_k * PSTRIDE;
+    float f[kSplitMaxK], lp[kSplitMaxK];
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kSplitMaxK; ++q) {
+        if (q < sp_k) {
+            const float2 lm = __ldcg(reinterpret_cast<const float2*>(base + q * PSTRIDE + PART_LM) + tid);
+            lp[q] = lm.x;
+            f[q] = lm.y;
+            M = fmaxf(M, lm.y);
+        }
+    }
+    float l = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kSplitMaxK; ++q) {
+        if (q < sp_k) {
+            f[q] = exp2_int(f[q] - M);
+            l += lp[q] * f[q];
+        }
+    }
+    const float oscale = scale_v / l;
+    uint16_t* orow = so.out;
+#pragma unroll 1
+    for (int c = 0; c < PART_CHUNKS; c += 2) {
+        const int d0 = cbase + 4 * c;
+        if (d0 + 8 > so.D) break;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kSplitMaxK; ++q) {
+            if (q < sp_k) {
+                const uint4* src = reinterpret_cast<const uint4*>(base + q * PSTRIDE);
+                const uint4 a = __ldcg(src + c * 256 + tid);
+                const uint4 b = __ldcg(src + (c + 1) * 256 + tid);
+                acc[0] += __uint_as_float(a.x) * f[q];
+                acc[1] += __uint_as_float(a.y) * f[q];
+                acc[2] += __uint_as_float(a.z) * f[q];
+                acc[3] += __uint_as_float(a.w) * f[q];
+                acc[4] += __uint_as_float(b.x) * f[q];
+                acc[5] += __uint_as_float(b.y) * f[q];
+                acc[6] += __uint_as_float(b.z) * f[q];
+                acc[7] += __uint_as_float(b.w) * f[q];
+            }
+        }
+        if (!row_valid || !VF_IN(so.out_off + d0, 8, so.out_elems, err)) continue;
+        uint4 v;
+        v.x = cvt_bf16x2(acc[0] * oscale, acc[1] * oscale);
+        v.y = cvt_bf16x2(acc[2] * oscale, acc[3] * oscale);
+        v.z = cvt_bf16x2(acc[4] * oscale, acc[5] * oscale);
+        v.w = cvt_bf16x2(acc[6] * oscale, acc[7] * oscale);
+        *reinterpret_cast<uint4*>(orow + d0) = v;
+    }
+}
 
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using namespace fa;
-    const int item = blockIdx.x;
+    // ---- CTA -> work item and key-range part.  Items from split_first on are
+    // cut into split_k parts of consecutive key tiles, one CTA each.
+    // Every load the decode needs goes out at once: the header (item count
+    // and split), and with at most 32 segments each lane's record.
+    const int cta = blockIdx.x;
+    const int4 mine = find_item_load(p);
+    const int4 hdr = *reinterpret_cast<const int4*>(p.ws);   // error, total_items, num_seqs, split_first
+    const int split_k = p.ws->split_k;
+    const int total = hdr.y;
+    const int split_first = hdr.w;
+    int item = cta, part = 0, nparts = 1;
+    if (split_k > 1 && cta >= split_first) {
+        const int d = cta - split_first;
+        item = split_first + d / split_k;
+        part = d - (d / split_k) * split_k;
+        nparts = split_k;
+    }
     // ---- work item -> (segment, head, query tile): one record of the work list
     SegRec rec;
-    int total;
-    if (!find_item(p, item, rec, total) || item >= total) return;
+    if (item >= total || !find_item_pick(p, item, mine, rec)) return;
     const int local = item - rec.first_item;
     const int seg_s = rec.seg_s;
     const int seg_e = rec.seg_e;
@@ -165,7 +322,17 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int qt = local - h * nq;
     const int q0 = seg_s + qt * ROWS_PER_ITEM;
     const int kbase = seg_s & ~15;
-    const int nkv = (seg_e - kbase + BN - 1) / BN;
+    const int nkv_all = (seg_e - kbase + BN - 1) / BN;
+    // This part's key tiles t0 .. t0 + nkv - 1 (all of them when not split;
+    // the plan gives every part at least one).
+    const int t0 = nkv_all * part / nparts;
+    const int nkv = nkv_all * (part + 1) / nparts - t0;
+    const int kb0 = kbase + t0 * BN;
+    if (VF_CHECKED_BUILD && (nkv < 1 || (nparts > 1 && (item - split_first >= kSplitMaxParts ||
+                                                         cta - split_first >= kSplitMaxParts)))) {
+        if (threadIdx.x == 0) record_error(&p.ws->error, VITFP8_ERR_DEVICE_BOUNDS);
+        return;
+    }
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -177,6 +344,14 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        // For the epilogue (read after the set-up sync, so that these values
+        // do not stay live through the tile loop): split slot, split item, parts.
+        int* spl = reinterpret_cast<int*>(smem + SM_SPLIT);
+        spl[0] = cta - split_first;
+        spl[1] = item - split_first;
+        spl[2] = nparts;
+    }
 
     // The TMA thread initialises the barriers and starts the copies the first
     // S product needs (the Q tile and K tile 0) at once, so they are in flight
@@ -187,11 +362,11 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     auto load_k = [&](int j) {
         const int s = j % NST;
         mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
-        tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, kbase + j * BN);
+        tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, h, kb0 + j * BN);
     };
     auto load_v = [&](int j) {
         const int s = j % NST;
-        const int key0 = kbase + j * BN;
+        const int key0 = kb0 + j * BN;
         mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
         tma_load_3d(sb + SM_V + s * VBYTES, &tmV, BAR(B_VFULL + s), key0, 0, h);
         tma_load_3d(sb + SM_V + s * VBYTES + VBLK, &tmV, BAR(B_VFULL + s), key0 + HALF, 0, h);
@@ -216,9 +391,9 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tma_prefetch_desc(&tmV);
         mbar_arrive_expect_tx(BAR(B_QFULL), QBYTES);
         tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, h, q0);
-        // V^T copies start at token kbase + j * BN, a multiple of 16: TMA needs
+        // V^T copies start at token kb0 + j * BN, a multiple of 16: TMA needs
         // the innermost coordinate 16-byte aligned (checked in the checked build).
-        if (VF_CHECKED_BUILD && (kbase & 15) != 0) {
+        if (VF_CHECKED_BUILD && (kb0 & 15) != 0) {
             record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
             *abort_flag = 1;
         } else {
@@ -263,7 +438,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
                 // The Q tile and K tile 0 are in flight since the set-up
-                // (neither K nor V if the set-up found kbase misaligned): V
+                // (neither K nor V if the set-up found kb0 misaligned): V
                 // tile 0 and K/V tiles 1..NST-1 go at once, while the other
                 // warps finish their set-up; tile j >= NST reuses its stage
                 // once S and P.V of tile j - NST are done with it.
@@ -403,7 +578,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SFREE));
 
-            const int key0 = kbase + j * BN + half * HALF;
+            const int key0 = kb0 + j * BN + half * HALF;
             float pmax = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             if (key0 < seg_s || key0 + HALF > seg_e) {
                 // First or last tile: keys outside the segment are masked, and
@@ -492,32 +667,51 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (lane == 0) mbar_arrive(BAR(B_PFULL));
         }
         if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL), (nkv - 1) & 1, abort_flag, err));
-        if (ok) {
-            tc_fence_after();
-            uint32_t lbits;   // both halves: a copy of l (column DV)
-            uint32_t oa[32], ob[32], oc[16];
-            tmem_ld_o80<OSPLIT>(tO, tO + uint32_t(p.DV), oa, ob, oc, lbits);
-            const float oscale = scale_v / __uint_as_float(lbits);
-            uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
-            const int cbase = half * OSPLIT;
-            auto store8 = [&](int d0, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
-                              uint32_t a5, uint32_t a6, uint32_t a7) {
-                if (!row_valid || d0 + 8 > p.D) return;
-                if (!VF_IN((int64_t(qrow) * p.H + h) * p.D + d0, 8, p.out_elems, err)) return;
-                uint4 v;
-                v.x = cvt_bf16x2(__uint_as_float(a0) * oscale, __uint_as_float(a1) * oscale);
-                v.y = cvt_bf16x2(__uint_as_float(a2) * oscale, __uint_as_float(a3) * oscale);
-                v.z = cvt_bf16x2(__uint_as_float(a4) * oscale, __uint_as_float(a5) * oscale);
-                v.w = cvt_bf16x2(__uint_as_float(a6) * oscale, __uint_as_float(a7) * oscale);
-                *reinterpret_cast<uint4*>(orow + d0) = v;
-            };
+        uint16_t* orow = p.out + (int64_t(qrow) * p.H + h) * p.D;
+        const int cbase = half * OSPLIT;
+        // Eight output columns d0..d0+7 of this row: o = O * oscale, rounded to bf16.
+        auto store8 = [&](int d0, float oscale, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                          uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+            if (!row_valid || d0 + 8 > p.D) return;
+            if (!VF_IN((int64_t(qrow) * p.H + h) * p.D + d0, 8, p.out_elems, err)) return;
+            uint4 v;
+            v.x = cvt_bf16x2(__uint_as_float(a0) * oscale, __uint_as_float(a1) * oscale);
+            v.y = cvt_bf16x2(__uint_as_float(a2) * oscale, __uint_as_float(a3) * oscale);
+            v.z = cvt_bf16x2(__uint_as_float(a4) * oscale, __uint_as_float(a5) * oscale);
+            v.w = cvt_bf16x2(__uint_as_float(a6) * oscale, __uint_as_float(a7) * oscale);
+            *reinterpret_cast<uint4*>(orow + d0) = v;
+        };
+        const int* spl = reinterpret_cast<const int*>(smem + SM_SPLIT);
+        const int sp_k = spl[2];   // parts of this CTA's work item (1: not split)
+        if (sp_k == 1) {
+            if (ok) {
+                tc_fence_after();
+                uint32_t lbits;   // both halves: a copy of l (column DV)
+                uint32_t oa[32], ob[32], oc[16];
+                tmem_ld_o80<OSPLIT>(tO, tO + uint32_t(p.DV), oa, ob, oc, lbits);
+                const float oscale = scale_v / __uint_as_float(lbits);
 #pragma unroll
-            for (int q = 0; q < 32; q += 8) {
-                store8(cbase + q, oa[q], oa[q + 1], oa[q + 2], oa[q + 3], oa[q + 4], oa[q + 5], oa[q + 6], oa[q + 7]);
-                store8(cbase + 32 + q, ob[q], ob[q + 1], ob[q + 2], ob[q + 3], ob[q + 4], ob[q + 5], ob[q + 6], ob[q + 7]);
+                for (int q = 0; q < 32; q += 8) {
+                    store8(cbase + q, oscale, oa[q], oa[q + 1], oa[q + 2], oa[q + 3], oa[q + 4], oa[q + 5],
+                           oa[q + 6], oa[q + 7]);
+                    store8(cbase + 32 + q, oscale, ob[q], ob[q + 1], ob[q + 2], ob[q + 3], ob[q + 4],
+                           ob[q + 5], ob[q + 6], ob[q + 7]);
+                }
+                store8(cbase + 64, oscale, oc[0], oc[1], oc[2], oc[3], oc[4], oc[5], oc[6], oc[7]);
+                store8(cbase + 72, oscale, oc[8], oc[9], oc[10], oc[11], oc[12], oc[13], oc[14], oc[15]);
             }
-            store8(cbase + 64, oc[0], oc[1], oc[2], oc[3], oc[4], oc[5], oc[6], oc[7]);
-            store8(cbase + 72, oc[8], oc[9], oc[10], oc[11], oc[12], oc[13], oc[14], oc[15]);
+        } else {
+            SplitOut so;
+            so.part = p.split_part;
+            so.cnt = p.split_cnt;
+            so.out = orow;
+            so.err = err;
+            so.out_off = (int64_t(qrow) * p.H + h) * p.D;
+            so.out_elems = p.out_elems;
+            so.D = p.D;
+            so.DV = p.DV;
+            split_part_epilogue(so, tO, row_valid, half, m_ref, scale_v, spl[0], spl[1], sp_k, ok, abort_flag,
+                                smem + SM_LAST);
         }
     }
 
@@ -535,8 +729,15 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // there are at most 2048; in cu_seqlens order otherwise), items per segment =
 // ceil(L / rows_per_item) * H, each record's first_item the items of all
 // records before it (a block-wide scan, 1024 records per step).
+//
+// Key-range split (split_bn > 0): N items on nsm SMs leave r = N mod nsm items
+// for a last wave that would hold the GPU for a whole item while most SMs
+// idle.  When r <= nsm / 2, each of those r items is cut into k = nsm / r
+// parts (at most kSplitMaxK, at most kSplitMaxParts CTAs, and no more parts
+// than the item has key tiles of split_bn keys), one CTA per part.
 __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T, int H,
-                                 int rows_per_item, WsHeader* ws, SegRec* rec) {
+                                 int rows_per_item, int nsm, int split_bn, WsHeader* ws,
+                                 SegRec* rec, int32_t* split_cnt) {
     __shared__ int bad;
     __shared__ int warp_sum[32];
     __shared__ int carry;
@@ -545,6 +746,8 @@ __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T
         bad = (cu[0] != 0 || cu[nseq] != T) ? 1 : 0;
         carry = 0;
     }
+    if (split_cnt != nullptr)
+        for (int i = threadIdx.x; i < kSplitMaxParts; i += blockDim.x) split_cnt[i] = 0;
     __syncthreads();
     for (int b = threadIdx.x; b < nseq; b += blockDim.x)
         if (cu[b + 1] < cu[b]) atomicOr(&bad, 1);
@@ -553,6 +756,8 @@ __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T
         if (threadIdx.x == 0) {
             ws->total_items = 0;
             ws->num_seqs = nseq;
+            ws->split_first = 0;
+            ws->split_k = 1;
             record_error(&ws->error, VITFP8_ERR_BAD_SEQLENS);
         }
         return;
@@ -602,8 +807,28 @@ __global__ void attn_plan_kernel(const int32_t* __restrict__ cu, int nseq, int T
         __syncthreads();
     }
     if (threadIdx.x == 0) {
-        ws->total_items = carry;
+        const int N = carry;
+        int sfirst = N, sk = 1;
+        const int r = nsm > 0 ? N % nsm : 0;
+        if (split_bn > 0 && split_cnt != nullptr && r > 0 && 2 * r <= nsm) {
+            int k = min(min(nsm / r, kSplitMaxK), kSplitMaxParts / r);
+            // Every part needs a key tile of its own: the segments of items N-r..N-1.
+            for (int b = nseq - 1; b >= 0; --b) {
+                if (!VF_IN(b, 1, nseq, &ws->error)) break;
+                const SegRec R = rec[b];
+                if (R.nq == 0) continue;
+                if (R.first_item + R.nq * H <= N - r) break;
+                k = min(k, (R.seg_e - (R.seg_s & ~15) + split_bn - 1) / split_bn);
+            }
+            if (k >= 2) {
+                sfirst = N - r;
+                sk = k;
+            }
+        }
+        ws->total_items = N;
         ws->num_seqs = nseq;
+        ws->split_first = sfirst;
+        ws->split_k = sk;
     }
 }
 
@@ -648,10 +873,13 @@ PerDeviceOnce g_smem_attr;
 }  // namespace
 
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
-                             void* ws, cudaStream_t s) {
+                             int nsm, int split_bn, void* ws, cudaStream_t s) {
     WsHeader* hdr = static_cast<WsHeader*>(ws);
-    attn_plan_kernel<<<1, 1024, 0, s>>>(cu, nseq, T, H, rows_per_item, hdr,
-                                        reinterpret_cast<SegRec*>(hdr + 1));
+    int32_t* cnt = split_bn > 0 ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
+                                                             ws_split_cnt_offset(nseq))
+                                : nullptr;
+    attn_plan_kernel<<<1, 1024, 0, s>>>(cu, nseq, T, H, rows_per_item, nsm, split_bn, hdr,
+                                        reinterpret_cast<SegRec*>(hdr + 1), cnt);
     return cudaGetLastError();
 }
 
@@ -670,10 +898,13 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
                         uint64_t(Tv) * Dp, HALF, uint32_t(DV), 1))
         return VITFP8_ERR_CUDA;
 
-    if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, ws, s) != cudaSuccess) return VITFP8_ERR_CUDA;
+    int dev = -1, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return VITFP8_ERR_CUDA;
+    if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, nsm, BN, ws, s) != cudaSuccess)
+        return VITFP8_ERR_CUDA;
 
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return VITFP8_ERR_CUDA;
     if (!g_smem_attr.run(dev, [] {
             return cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         SMEM_BYTES) == cudaSuccess;
@@ -686,6 +917,8 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     prm.ws = hdr;
     prm.st = st;
     prm.out = out;
+    prm.split_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + ws_split_cnt_offset(nseq));
+    prm.split_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ws_split_part_offset(nseq));
     prm.nseq = nseq;
     prm.T = T;
     prm.H = H;
@@ -695,7 +928,9 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     prm.KS = (D + 31) / 32;
     prm.sm_scale = sm_scale;
     prm.out_elems = int64_t(T) * H * D;
-    const long long grid = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H;
+    // Work items are at most (T / 128 + nseq) * H; a split adds at most
+    // kSplitMaxParts CTAs.  CTAs past the call's count return at once.
+    const long long grid = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H + kSplitMaxParts;
     if (grid > 0x7FFFFFFFLL) return VITFP8_ERR_UNSUPPORTED;
     attn_fp8_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;

@@ -25,9 +25,9 @@
 namespace {
 
 constexpr int32_t kMaxSeqs = VITFP8_NOALLOC_MAX_SEQS;
-// Same layout as a caller workspace: 64-byte header, one 16-byte record per segment.
-constexpr size_t kScratchBytes =
-    (sizeof(vitfp8::WsHeader) + sizeof(vitfp8::SegRec) * size_t(kMaxSeqs) + 255) & ~size_t(255);
+// Same layout as a caller workspace: 64-byte header, one 16-byte record per
+// segment, the key-range split's counters and partial results.
+constexpr size_t kScratchBytes = vitfp8::ws_bytes(kMaxSeqs);
 
 static __device__ __align__(256) uint8_t g_attn_scratch[kScratchBytes];
 

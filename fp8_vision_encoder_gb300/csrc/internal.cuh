@@ -19,12 +19,15 @@ struct SrcDev {
 
 // Attention workspace: a header, then one record per segment in the work
 // list's order (longest first), so that a CTA finds its segment with one
-// 16-byte load per probe.
+// 16-byte load per probe; then the key-range split's arrival counters and
+// partial results (FP8 kernel only).
 struct WsHeader {
     int32_t error;        // first device-detected vitfp8_status
     int32_t total_items;  // work items of the current call
     int32_t num_seqs;
-    int32_t pad[13];
+    int32_t split_first;  // first work item whose key range is split (total_items: none)
+    int32_t split_k;      // parts per split item (1: none)
+    int32_t pad[11];
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 
@@ -35,9 +38,21 @@ struct SegRec {
 };
 static_assert(sizeof(SegRec) == 16, "one 16-byte load per record");
 
-inline size_t ws_bytes(int32_t num_seqs) {
-    size_t b = sizeof(WsHeader) + sizeof(SegRec) * size_t(num_seqs);
-    return (b + 255) & ~size_t(255);
+// Key-range split of the last, partly filled wave of work items: at most
+// kSplitMaxParts CTAs (one wave) and kSplitMaxK parts per item; each part
+// leaves kSplitPartBytes of partial results.
+constexpr int kSplitMaxParts = 160;
+constexpr int kSplitMaxK = 4;
+constexpr size_t kSplitPartBytes = 84 * 1024;
+
+constexpr size_t ws_rec_bytes(int32_t num_seqs) {
+    return (sizeof(WsHeader) + sizeof(SegRec) * size_t(num_seqs) + 255) & ~size_t(255);
+}
+constexpr size_t ws_split_cnt_offset(int32_t num_seqs) { return ws_rec_bytes(num_seqs); }
+constexpr size_t ws_split_part_offset(int32_t num_seqs) { return ws_rec_bytes(num_seqs) + 1024; }
+static_assert(kSplitMaxParts * sizeof(int32_t) <= 1024, "split counters fit their block");
+constexpr size_t ws_bytes(int32_t num_seqs) {
+    return ws_split_part_offset(num_seqs) + size_t(kSplitMaxParts) * kSplitPartBytes;
 }
 
 __device__ __forceinline__ void record_error(int32_t* word, int32_t code) {
@@ -64,8 +79,10 @@ cudaError_t launch_selftest_wait(void* ws, cudaStream_t s);
 cudaError_t launch_selftest_bounds(void* ws, cudaStream_t s);
 
 // ---- launchers (attn_fp8.cu)
+// split_bn > 0 and nsm > 0 let the plan split the key ranges (tiles of
+// split_bn keys) of the last wave's items over up to nsm CTAs.
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
-                             void* ws, cudaStream_t s);
+                             int nsm, int split_bn, void* ws, cudaStream_t s);
 vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
                               const vitfp8_scale_state* st, const int32_t* cu, int nseq, int T,
                               int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,

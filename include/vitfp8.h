@@ -248,9 +248,17 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs);
  * D: 8..128, D % 8 == 0; D_pad % 16 == 0, D <= D_pad <= 128.
  * sm_scale: softmax scale, normally 1/sqrt(D); finite and > 0.
  * out: bf16 [T][H][D].
- * d_workspace: >= vitfp8_attn_workspace_size(num_seqs) bytes, 16-byte
- *          aligned; holds the (longest-first) work list and an error word.
- *          Calls sharing one workspace must be stream-ordered.
+ * d_workspace: >= vitfp8_attn_workspace_size(num_seqs) bytes (about 14 MB),
+ *          16-byte aligned; holds the (longest-first) work list, an error
+ *          word and the partial results of a key-range split.  Calls sharing
+ *          one workspace must be stream-ordered.
+ *
+ * Scheduling: one CTA per 128-query tile of a (segment, head).  When the
+ * tiles leave a last wave that fills at most half the GPU, the key range of
+ * each of those tiles is split over up to 4 CTAs, and the CTA that finishes
+ * last combines the parts by exact powers of two (same numerics up to the
+ * fp32 summation order); the result is deterministic for a given input and
+ * GPU.
  */
 vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
                                  const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,
@@ -300,9 +308,10 @@ vitfp8_status vitfp8_attn_varlen_bf16(const vitfp8_bf16* q, const vitfp8_bf16* k
  * synchronisation that cudaMalloc may cause.
  *
  * Arguments, layouts and the computation are exactly those of
- * vitfp8_attn_varlen.  The work list lives instead in a fixed device array
- * inside the library (about 64 KB; every GPU that loads the library keeps it
- * until the process exits), sized for at most VITFP8_NOALLOC_MAX_SEQS
+ * vitfp8_attn_varlen.  The workspace (work list, error word and the partial
+ * results of a key-range split) lives instead in a fixed device array inside
+ * the library (about 14 MB; every GPU that loads the library keeps it until
+ * the process exits), sized for at most VITFP8_NOALLOC_MAX_SEQS
  * segments: num_seqs above that returns VITFP8_ERR_UNSUPPORTED without
  * launching.  The first call on each device looks up that array's device
  * address (cudaGetSymbolAddress) with the device current; make that first
