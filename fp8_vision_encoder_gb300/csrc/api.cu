@@ -200,7 +200,7 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
         return VITFP8_ERR_INVALID_ARG;
     if (!d_workspace || !aligned16(d_workspace) || workspace_bytes < ws_bytes(num_seqs))
         return VITFP8_ERR_WORKSPACE;
-    return launch_attn_fp8(q8, k8, v8t, d_state, d_cu_seqlens, num_seqs, total_tokens, H, D, D_pad,
+    return launch_attn_fp8(q8, k8, v8t, d_state, d_cu_seqlens, num_seqs, max_seqlen, total_tokens, H, D, D_pad,
                            vitfp8_vt_stride(total_tokens), sm_scale,
                            reinterpret_cast<uint16_t*>(out), d_workspace, stream);
 }

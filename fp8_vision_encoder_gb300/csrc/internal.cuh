@@ -27,7 +27,8 @@ struct WsHeader {
     int32_t num_seqs;
     int32_t split_first;  // first work item whose key range is split (total_items: none)
     int32_t split_k;      // parts per split item (1: none)
-    int32_t pad[11];
+    int32_t next_unit;    // FP8 kernel: units handed out beyond the first wave (zeroed by the plan)
+    int32_t pad[10];
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 
@@ -83,9 +84,11 @@ cudaError_t launch_selftest_bounds(void* ws, cudaStream_t s);
 // split_bn keys) of the last wave's items over up to nsm CTAs.
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
                              int nsm, int split_bn, void* ws, cudaStream_t s);
+// max_seqlen (>= every segment's length) picks the kernel: persistent for
+// short segments, one work item per CTA otherwise (same results).
 vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
-                              const vitfp8_scale_state* st, const int32_t* cu, int nseq, int T,
-                              int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,
+                              const vitfp8_scale_state* st, const int32_t* cu, int nseq, int max_seqlen,
+                              int T, int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,
                               void* ws, cudaStream_t s);
 
 // ---- launcher (attn_bf16.cu)

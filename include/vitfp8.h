@@ -253,12 +253,14 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs);
  *          word and the partial results of a key-range split.  Calls sharing
  *          one workspace must be stream-ordered.
  *
- * Scheduling: one CTA per 128-query tile of a (segment, head).  When the
- * tiles leave a last wave that fills at most half the GPU, the key range of
- * each of those tiles is split over up to 4 CTAs, and the CTA that finishes
- * last combines the parts by exact powers of two (same numerics up to the
- * fp32 summation order); the result is deterministic for a given input and
- * GPU.
+ * Scheduling: one work unit per 128-query tile of a (segment, head).  When
+ * the tiles leave a last wave that fills at most half the GPU, the key range
+ * of each of those tiles is split over up to 4 units, and the unit that
+ * finishes last combines the parts by exact powers of two (same numerics up
+ * to the fp32 summation order); the result is deterministic for a given input
+ * and GPU.  With max_seqlen <= 6144 a persistent kernel (one CTA per SM)
+ * runs the units, otherwise one CTA per unit; both give the same bits, so
+ * max_seqlen affects only the speed.
  */
 vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
                                  const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,

@@ -89,6 +89,7 @@ def run_cases(vf):
         ("padded", [5, 300, 77], 3, 80, 43, True, "padded"),
         ("fused", [257, 31], 4, 128, 44, True, "fused"),
         ("split", [2048, 600], 2, 128, 45, True, "packed"),   # every item's key range split
+        ("long", [7000, 300], 1, 128, 46, True, "packed"),    # one CTA per work item (segments > 6144)
     ]
     for D in range(8, 129, 8):
         cases.append(("d%d" % D, [3, 130, 61], 2, D, 100 + D, D % 16 == 0, "packed"))

@@ -1,0 +1,61 @@
+"""The FP8 attention call runs one of two kernels, chosen by max_seqlen: a
+persistent one (one CTA per SM walking the work units, for segments of up to
+6144 tokens) and one with a CTA per work item (longer segments).  Both do the
+same arithmetic for every unit, so their outputs are bit-identical.  max_seqlen
+is only an upper bound on the segment lengths, so passing a larger one runs
+the other kernel on the same inputs; the first call of each case runs the
+persistent kernel and is also checked against the fp64 oracle.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import assert_attention_ok, compare_attention, cu_tensor, oracle_push, vt_to_thd
+from oracle import scales as oscales
+
+pytestmark = pytest.mark.gpu
+
+PERSISTENT_MAX = 6144
+
+
+@pytest.fixture(scope="module")
+def vf():
+    import fp8_vision_encoder_gb300 as vf
+    assert torch.cuda.is_available()
+    return vf
+
+
+CASES = [
+    ("ragged", [1, 127, 128, 129, 300, 17, 0, 5], 2, 128),
+    ("hd_like", [3600, 3600, 3600], 4, 80),
+    ("split_all", [2048], 2, 128),                 # every item's key range split
+    ("many_short", [256] * 200, 4, 64),            # ~5 units per CTA
+    ("near_threshold", [6000, 100, 44], 1, 128),
+]
+
+
+@pytest.mark.parametrize("name,seqlens,H,D", CASES, ids=[c[0] for c in CASES])
+def test_kernels_agree_bitwise(vf, name, seqlens, H, D):
+    assert max(seqlens) <= PERSISTENT_MAX
+    cu, cul = cu_tensor(seqlens)
+    st = vf.ScaleState().init()
+    ost = oscales.ScaleState()
+    q, k, v = [t.cuda() for t in workloads.make_qkv(seqlens, H, D, 90 + len(name), True, False, device="cpu")]
+    vf.amax_update(st, q, k, v, cu)
+    oracle_push(ost, q, k, v)
+    q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
+    outs = []
+    for max_seqlen in (max(seqlens), 1 << 20):
+        ws = vf.Workspace(len(seqlens))
+        outs.append(vf.attn_varlen(q8, k8, v8t, st, cu, max_seqlen, D, workspace=ws))
+        torch.cuda.synchronize()
+        assert ws.error() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    T = sum(seqlens)
+    rows = None
+    if T > 4000:
+        rows = np.random.default_rng(5).choice(T, 1500, replace=False)
+    stats = compare_attention(outs[0], q8, k8, vt_to_thd(v8t, T), list(ost.scale), cul, D, rows=rows)
+    assert_attention_ok(stats, name, True)
