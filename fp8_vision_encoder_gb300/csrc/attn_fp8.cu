@@ -14,7 +14,7 @@
 // unit's Q and K/V tiles while the current unit finishes, so a unit's set-up
 // and first loads overlap the previous unit's last tiles.  The host takes the
 // persistent kernel for segments of up to 6144 tokens, where that fixed cost
-// weighs most.  Roles:
+// weighs most, when there is more than one wave of work items.  Roles:
 //
 //   warp 8      TMA producer: the Q tile once, then K tiles (256 keys x 128 d)
 //               and V^T tiles (d x 256 keys) through a shared-memory ring
@@ -1448,7 +1448,10 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     // (T / 128 + nseq) * H + kSplitMaxParts; CTAs without a unit return at once.
     const long long max_units = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H + kSplitMaxParts;
     if (max_units > 0x7FFFFFFFLL) return VITFP8_ERR_UNSUPPORTED;
-    if (max_seqlen <= kPersistentMaxSeqlen) {
+    // Work items are at most (T / 128 + nseq) * H; with no more than one wave
+    // of them there is no next unit to overlap.
+    const long long max_items = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H;
+    if (max_seqlen <= kPersistentMaxSeqlen && max_items > nsm) {
         // Short segments: one CTA per SM walking the units, so a unit's set-up
         // and first loads overlap the previous unit's last tiles.
         const unsigned grid = unsigned(max_units < nsm ? max_units : nsm);

@@ -258,9 +258,9 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs);
  * of each of those tiles is split over up to 4 units, and the unit that
  * finishes last combines the parts by exact powers of two (same numerics up
  * to the fp32 summation order); the result is deterministic for a given input
- * and GPU.  With max_seqlen <= 6144 a persistent kernel (one CTA per SM)
- * runs the units, otherwise one CTA per unit; both give the same bits, so
- * max_seqlen affects only the speed.
+ * and GPU.  With max_seqlen <= 6144 and more than one wave of work items a
+ * persistent kernel (one CTA per SM) runs the units, otherwise one CTA per
+ * unit; both give the same bits, so max_seqlen affects only the speed.
  */
 vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
                                  const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,

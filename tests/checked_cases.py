@@ -90,6 +90,7 @@ def run_cases(vf):
         ("fused", [257, 31], 4, 128, 44, True, "fused"),
         ("split", [2048, 600], 2, 128, 45, True, "packed"),   # every item's key range split
         ("long", [7000, 300], 1, 128, 46, True, "packed"),    # one CTA per work item (segments > 6144)
+        ("psplit", [2048], 12, 128, 47, True, "packed"),      # persistent kernel, last wave split
     ]
     for D in range(8, 129, 8):
         cases.append(("d%d" % D, [3, 130, 61], 2, D, 100 + D, D % 16 == 0, "packed"))

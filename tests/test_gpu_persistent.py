@@ -1,6 +1,7 @@
 """The FP8 attention call runs one of two kernels, chosen by max_seqlen: a
 persistent one (one CTA per SM walking the work units, for segments of up to
-6144 tokens) and one with a CTA per work item (longer segments).  Both do the
+6144 tokens when there is more than one wave of work items) and one with a
+CTA per work item (longer segments, or a single wave).  Both do the
 same arithmetic for every unit, so their outputs are bit-identical.  max_seqlen
 is only an upper bound on the segment lengths, so passing a larger one runs
 the other kernel on the same inputs; the first call of each case runs the
@@ -27,12 +28,14 @@ def vf():
     return vf
 
 
+# Every case has more work items than a GB300 has SMs (the persistent kernel
+# runs only then: with a single wave there is no next unit to overlap).
 CASES = [
-    ("ragged", [1, 127, 128, 129, 300, 17, 0, 5], 2, 128),
+    ("ragged", [1, 127, 128, 129, 300, 17, 0, 5], 16, 128),
     ("hd_like", [3600, 3600, 3600], 4, 80),
-    ("split_all", [2048], 2, 128),                 # every item's key range split
+    ("split_last_wave", [2048], 12, 128),          # 192 items: the last 40 split in 3
     ("many_short", [256] * 200, 4, 64),            # ~5 units per CTA
-    ("near_threshold", [6000, 100, 44], 1, 128),
+    ("near_threshold", [6000, 100, 44], 4, 128),
 ]
 
 
