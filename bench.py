@@ -142,6 +142,15 @@ class ClockSampler:
 L2_FLUSH_BYTES = 256 << 20   # twice the GB300's L2
 
 
+def flush_l2(buf, value=1):
+    """Evict the L2 outside a timed span: write a buffer twice its size, then
+    read it all back, so that the lines left in the L2 are clean.  (After the
+    write alone the L2 holds ~129 MB of dirty lines, and the next kernel pays
+    for writing them back: ~15 us on the first kernel of a short span.)"""
+    buf.fill_(value)
+    buf.view(torch.int32).max()
+
+
 def clocks_rejected(clocks):
     """True for a clock record the timing rules reject: hw_slowdown,
     hw_thermal_slowdown or sw_thermal_slowdown active, or the median SM clock
@@ -351,7 +360,7 @@ def resolution_sweep(vf, dev, stream, reps, head_dims=(80, 128), H=16, images=3,
                     fn()
                 times = []
                 for _ in range(reps):
-                    flush.fill_(1)
+                    flush_l2(flush)
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
                     fn()
@@ -385,8 +394,8 @@ def per_config_block(vf, dev, stream, peaks, peak_kind, reps=None):
     """One layer of each PER_CONFIG workload as `bench.py --workload NAME` runs
     it (dynamic scaling = amax + ring + quantize; static = quantize), FP8
     attention and the BF16 path on the same inputs; each arm timed alone with
-    CUDA events, the L2 flushed (a 256 MB write, outside the timed span) before
-    every rep, median of the reps."""
+    CUDA events, the L2 flushed (a 256 MB write read back, outside the timed
+    span) before every rep, median of the reps."""
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
     bf16_peak = peaks["bf16_tflops_sustained"]
@@ -418,7 +427,7 @@ def per_config_block(vf, dev, stream, peaks, peak_kind, reps=None):
             times = []
             for _ in range(n):
                 with torch.cuda.stream(stream):
-                    flush.fill_(1)
+                    flush_l2(flush)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 fn()
@@ -451,7 +460,7 @@ def per_config_block(vf, dev, stream, peaks, peak_kind, reps=None):
     block["_peaks"] = {"fp8": fp8_peak, "bf16": bf16_peak, "hbm_gbs": peaks["hbm_gbs"],
                        "source": "%s bf16 sustained x %.0f for FP8; %s HBM copy"
                                  % (peak_kind, FP8_PER_BF16, peak_kind),
-                       "l2": "flushed (256 MB write) before every rep, outside the timed span"}
+                       "l2": "flushed (256 MB write, read back) before every rep, outside the timed span"}
     return block
 
 
@@ -527,7 +536,7 @@ def main():
         else:
             for s in range(args.steps):
                 with torch.cuda.stream(stream):
-                    flush.fill_(s & 0xFF)
+                    flush_l2(flush, s & 0xFF)
                 marks[s][0].record(stream)
                 run.step(stream, evs[s])
                 marks[s][1].record(stream)
@@ -578,7 +587,7 @@ def main():
                    "static_scales": run.static,
                    "l2": (("inputs larger than L2 (each layer reads its own %.0f MB of bf16 q/k/v)"
                            % (3 * w.T * w.H * w.D * 2 / 1e6)) if flush is None else
-                          ("L2 flushed (a %d MB write) before every timed step, outside the timed "
+                          ("L2 flushed (a %d MB write, read back) before every timed step, outside the timed "
                            "spans; a step reads %.0f MB of bf16 q/k/v" % (L2_FLUSH_BYTES >> 20,
                                                                           step_bytes / 1e6))),
                    "parallelism": "replicas" if ws > 1 else "single"},

@@ -44,11 +44,14 @@ __device__ __forceinline__ int64_t src_row_of(const SrcDev& L, const int32_t* cu
     return int64_t(lo) * L.s_max + i;
 }
 
+// Not volatile: the inputs are read-only for the kernel's duration, so the
+// compiler may hoist several of these loads ahead of the arithmetic that uses
+// them (they are then in flight together).
 __device__ __forceinline__ uint4 ld_stream16(const uint16_t* p) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
     return r;
 }
 
@@ -242,7 +245,11 @@ amax_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q, const uint16
 // (blocks, 1, 3); each block walks 16-token tiles, each warp two tokens of a
 // tile, 32 lanes x 16 bytes per step.
 constexpr int AR_TOK = 16;
-__global__ void __launch_bounds__(QT_THREADS)
+static_assert(AR_TOK == 2 * (QT_THREADS / 32), "two tokens of a tile per warp");
+// At least 4 resident blocks per SM: up to 64 registers, so that a warp's 16
+// loads of a tile are in flight together (at 8 blocks the compiler keeps to
+// 32 registers and a few loads at a time).
+__global__ void __launch_bounds__(QT_THREADS, 4)
 amax_rows_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q,
                  const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, SrcDev L,
                  const int32_t* __restrict__ cu, int nseq, int T, int H, int D,
@@ -268,25 +275,33 @@ amax_rows_kernel(vitfp8_scale_state* st, const uint16_t* __restrict__ q,
             rows[threadIdx.x] = t < T ? src_row_of(L, cu, nseq, t, &st->dev_error) : -1;
         }
         __syncthreads();
-        for (int tt = warp; tt < AR_TOK; tt += QT_THREADS / 32) {
-            const int64_t row = rows[tt];
-            if (row < 0) continue;
-            const uint16_t* p = src + row * L.ts;
-            for (int j = lane; j < RV; j += 4 * 32) {
-                uint4 w[4];
+        // Warp w reads tokens w and w + 8 of the tile: both rows' 16-byte
+        // vectors, 8 per lane and row, are in flight before any is reduced.
+        const int64_t rowA = rows[warp], rowB = rows[warp + QT_THREADS / 32];
+        for (int j0 = 0; j0 < RV; j0 += 8 * 32) {
+            uint4 w[16];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    w[u] = (j + 32 * u < RV &&
-                            VF_IN(row * L.ts + int64_t(j + 32 * u) * 8, 8, L.extent, &st->dev_error))
-                               ? ld_stream16(p + (j + 32 * u) * 8)
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + lane + 32 * u;
+                w[u] = (rowA >= 0 && j < RV &&
+                        VF_IN(rowA * L.ts + int64_t(j) * 8, 8, L.extent, &st->dev_error))
+                           ? ld_stream16(src + rowA * L.ts + int64_t(j) * 8)
+                           : make_uint4(0, 0, 0, 0);
+                w[8 + u] = (rowB >= 0 && j < RV &&
+                            VF_IN(rowB * L.ts + int64_t(j) * 8, 8, L.extent, &st->dev_error))
+                               ? ld_stream16(src + rowB * L.ts + int64_t(j) * 8)
                                : make_uint4(0, 0, 0, 0);
+            }
+            // Every load above is issued before the reduction starts.
+            asm volatile("" : "+r"(w[0].x), "+r"(w[1].x), "+r"(w[2].x), "+r"(w[3].x), "+r"(w[4].x), "+r"(w[5].x),
+                              "+r"(w[6].x), "+r"(w[7].x), "+r"(w[8].x), "+r"(w[9].x), "+r"(w[10].x), "+r"(w[11].x),
+                              "+r"(w[12].x), "+r"(w[13].x), "+r"(w[14].x), "+r"(w[15].x));
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    m = absmax_bf16x2(m, w[u].x);
-                    m = absmax_bf16x2(m, w[u].y);
-                    m = absmax_bf16x2(m, w[u].z);
-                    m = absmax_bf16x2(m, w[u].w);
-                }
+            for (int u = 0; u < 16; ++u) {
+                m = absmax_bf16x2(m, w[u].x);
+                m = absmax_bf16x2(m, w[u].y);
+                m = absmax_bf16x2(m, w[u].z);
+                m = absmax_bf16x2(m, w[u].w);
             }
         }
     }
@@ -485,9 +500,10 @@ cudaError_t launch_amax(vitfp8_scale_state* st, const uint16_t* q, const uint16_
                         const uint16_t* v, SrcDev L, const int32_t* cu, int nseq, int T, int H,
                         int D, float* out, cudaStream_t s) {
     if (L.hs == D) {
-        // about 8 resident blocks of 256 threads per SM, shared by the 3 tensors
+        // one 16-token tile per block up to 1024 blocks per tensor (about 4
+        // resident blocks of 256 threads per SM), then tiles walked by stride
         const int ntiles = (T + AR_TOK - 1) / AR_TOK;
-        dim3 grid(ntiles < 400 ? ntiles : 400, 1, 3);
+        dim3 grid(ntiles < 1024 ? ntiles : 1024, 1, 3);
         amax_rows_kernel<<<grid, QT_THREADS, 0, s>>>(st, q, k, v, L, cu, nseq, T, H, D, out);
     } else {
         dim3 grid((T + QT_TOK - 1) / QT_TOK, H, 3);
