@@ -25,10 +25,7 @@ from oracle import scales as oscales
 
 pytestmark = pytest.mark.gpu
 
-BN = 256            # keys per tile
-ROWS = 128          # queries per work item
-MAX_K = 4           # parts per item at most
-MAX_PARTS = 160     # split CTAs at most
+from split_rule import BN, ROWS, expected_split
 
 
 @pytest.fixture(scope="module")
@@ -40,30 +37,6 @@ def vf():
 
 def nsm():
     return torch.cuda.get_device_properties(0).multi_processor_count
-
-
-def expected_split(seqlens, H, n_sm):
-    """(total items, first split item, parts per item) as the plan decides them."""
-    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int64)
-    n = len(seqlens)
-    order = sorted(range(n), key=lambda b: (-seqlens[b], b)) if n <= 2048 else list(range(n))
-    first, recs = 0, []
-    for b in order:
-        nq = -(-seqlens[b] // ROWS)
-        recs.append((first, int(cu[b]), int(cu[b + 1]), nq))
-        first += nq * H
-    N = first
-    r = N % n_sm
-    if r == 0 or 2 * r > n_sm:
-        return N, N, 1
-    k = min(n_sm // r, MAX_K, MAX_PARTS // r)
-    for f, s, e, nq in reversed(recs):
-        if nq == 0:
-            continue
-        if f + nq * H <= N - r:
-            break
-        k = min(k, (e - (s & ~15) + BN - 1) // BN)
-    return (N, N - r, k) if k >= 2 else (N, N, 1)
 
 
 def _run(vf, seqlens, H, D, seed, outliers=True):
@@ -133,13 +106,3 @@ def test_split_ragged_and_deterministic(vf):
     torch.cuda.synchronize()
     for o in outs:
         assert torch.equal(o.view(torch.int16), r1["out"].view(torch.int16))
-
-
-def test_expected_split_rule_examples():
-    """The rule on fixed SM counts (no device state): a full last wave is not
-    split, a small one is, and no part is left without a key tile."""
-    assert expected_split([ROWS * 152], 1, 152) == (152, 152, 1)
-    assert expected_split([ROWS * 150, 600], 1, 152) == (155, 152, 3)
-    assert expected_split([2048], 2, 152) == (32, 0, 4)
-    assert expected_split([64, 192], 2, 152) == (6, 6, 1)        # one key tile per segment
-    assert expected_split([ROWS * 100], 1, 152) == (100, 100, 1)  # last wave more than half full
