@@ -46,8 +46,10 @@ def _call_noalloc(vf, q8, k8, v8t, st, cu, max_seqlen, D, out):
 def test_noalloc_matches_workspace_entry_point_twice():
     import fp8_vision_encoder_gb300 as vf
     assert torch.cuda.is_available()
-    # the third case's items are all split over several CTAs (key-range split)
-    cases = [([300, 129, 500], 2, 128, 31), ([1, 64, 700, 17, 3600], 3, 80, 32), ([2048], 2, 128, 34)]
+    # the third case's items are all split over several CTAs (key-range split);
+    # the fourth has more work items than SMs, so the persistent kernel runs it
+    cases = [([300, 129, 500], 2, 128, 31), ([1, 64, 700, 17, 3600], 3, 80, 32), ([2048], 2, 128, 34),
+             ([3600, 3600, 3600], 4, 80, 35)]
     for seqlens, H, D, seed in cases:
         cu, st, q8, k8, v8t = _inputs(vf, seqlens, H, D, seed)
         T = sum(seqlens)
