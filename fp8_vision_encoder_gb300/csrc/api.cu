@@ -223,7 +223,7 @@ vitfp8_status vitfp8_attn_varlen_bf16(const vitfp8_bf16* q, const vitfp8_bf16* k
     if (!d_workspace || !aligned16(d_workspace) || workspace_bytes < ws_bytes(num_seqs))
         return VITFP8_ERR_WORKSPACE;
     return launch_attn_bf16(reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k),
-                            reinterpret_cast<const uint16_t*>(v), d_cu_seqlens, num_seqs,
+                            reinterpret_cast<const uint16_t*>(v), d_cu_seqlens, num_seqs, max_seqlen,
                             total_tokens, H, D, sm_scale, reinterpret_cast<uint16_t*>(out),
                             d_workspace, stream);
 }

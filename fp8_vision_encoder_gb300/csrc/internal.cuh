@@ -93,7 +93,7 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
 
 // ---- launcher (attn_bf16.cu)
 vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                               const int32_t* cu, int nseq, int T, int H, int D, float sm_scale,
-                               uint16_t* out, void* ws, cudaStream_t s);
+                               const int32_t* cu, int nseq, int max_seqlen, int T, int H, int D,
+                               float sm_scale, uint16_t* out, void* ws, cudaStream_t s);
 
 }  // namespace vitfp8

@@ -284,7 +284,9 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
  *
  * q, k, v: bf16 [T][H][D], packed token order, rows contiguous (device).
  * D: 8..128, D % 8 == 0.  max_seqlen, sm_scale, out and d_workspace as for
- * vitfp8_attn_varlen (the same workspace size).
+ * vitfp8_attn_varlen (the same workspace size).  Scheduling as there, without
+ * the key-range split: a persistent kernel for max_seqlen <= 6144 and more
+ * than one wave of work items, one CTA per work item otherwise (same bits).
  * Errors: VITFP8_ERR_INVALID_ARG for bad sizes, null or misaligned (16-byte)
  * pointers; VITFP8_ERR_UNSUPPORTED for D > 128; VITFP8_ERR_WORKSPACE for a
  * missing or short workspace; malformed cu_seqlens and timed-out waits are

@@ -62,3 +62,18 @@ def test_kernels_agree_bitwise(vf, name, seqlens, H, D):
         rows = np.random.default_rng(5).choice(T, 1500, replace=False)
     stats = compare_attention(outs[0], q8, k8, vt_to_thd(v8t, T), list(ost.scale), cul, D, rows=rows)
     assert_attention_ok(stats, name, True)
+
+
+@pytest.mark.parametrize("name,seqlens,H,D", CASES, ids=[c[0] for c in CASES])
+def test_bf16_kernels_agree_bitwise(vf, name, seqlens, H, D):
+    """The BF16 path has the same two kernels and the same choice."""
+    cu, cul = cu_tensor(seqlens)
+    q, k, v = [t.cuda() for t in workloads.make_qkv(seqlens, H, D, 190 + len(name), True, False, device="cpu")]
+    outs = []
+    for max_seqlen in (max(seqlens), 1 << 20):
+        ws = vf.Workspace(len(seqlens))
+        outs.append(vf.attn_varlen_bf16(q, k, v, cu, max_seqlen, workspace=ws))
+        torch.cuda.synchronize()
+        assert ws.error() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
