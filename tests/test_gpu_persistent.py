@@ -77,3 +77,52 @@ def test_bf16_kernels_agree_bitwise(vf, name, seqlens, H, D):
         assert ws.error() == 0
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
+
+
+def _random_batches():
+    """Seeded random batches with more work items than SMs: up to 60
+    segments of 1..6000 tokens, 1..16 heads, a head dim of 32..128."""
+    rng = np.random.default_rng(2024)
+    out = []
+    while len(out) < 6:
+        n = int(rng.integers(1, 61))
+        seqlens = [int(x) for x in rng.integers(1, 6001, size=n)]
+        if rng.random() < 0.3:
+            seqlens[int(rng.integers(0, n))] = 0
+        H = int(rng.integers(1, 17))
+        D = int(rng.choice([32, 64, 80, 128]))
+        items = sum(-(-L // 128) for L in seqlens) * H
+        if items > 200 and sum(seqlens) * H * D < 40_000_000:
+            out.append((seqlens, H, D))
+    return out
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_random_batches_agree(vf, case):
+    """FP8 and BF16: the persistent kernel (max_seqlen = the true maximum) and
+    the per-item kernel (a larger bound) give the same bits on random batches."""
+    seqlens, H, D = _random_batches()[case]
+    cu, cul = cu_tensor(seqlens)
+    q, k, v = [t.cuda() for t in workloads.make_qkv(seqlens, H, D, 500 + case, True, False, device="cpu")]
+    st = vf.ScaleState().init()
+    ost = oscales.ScaleState()
+    vf.amax_update(st, q, k, v, cu)
+    oracle_push(ost, q, k, v)
+    q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
+    for bf16 in (False, True):
+        outs = []
+        for max_seqlen in (max(seqlens), 1 << 20):
+            ws = vf.Workspace(len(seqlens))
+            if bf16:
+                outs.append(vf.attn_varlen_bf16(q, k, v, cu, max_seqlen, workspace=ws))
+            else:
+                outs.append(vf.attn_varlen(q8, k8, v8t, st, cu, max_seqlen, D, workspace=ws))
+            torch.cuda.synchronize()
+            assert ws.error() == 0
+        assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), (case, bf16)
+        assert torch.isfinite(outs[0].float()).all()
+        if not bf16:
+            T = sum(seqlens)
+            rows = np.random.default_rng(case).choice(T, min(T, 300), replace=False)
+            stats = compare_attention(outs[0], q8, k8, vt_to_thd(v8t, T), list(ost.scale), cul, D, rows=rows)
+            assert_attention_ok(stats, "random batch %d" % case, True)
