@@ -50,7 +50,7 @@ def _peaks():
 
 # Source files each profiled kernel is compiled from (the summaries under
 # profiles/ record a hash over them).
-ATTN_FP8_SOURCES = ["attn_fp8.cu", "attn_common.cuh", "checked.cuh", "internal.cuh", "ptx.cuh"]
+ATTN_FP8_SOURCES = ["attn_fp8.cu", "attn_fp8_2tile.cu", "attn_common.cuh", "checked.cuh", "internal.cuh", "ptx.cuh"]
 QUANT_SOURCES = ["quant.cu", "checked.cuh", "internal.cuh", "ptx.cuh"]
 
 

@@ -41,6 +41,8 @@ STATUS_NAMES = {
     6: "VITFP8_ERR_BAD_SEQLENS", 7: "VITFP8_ERR_WORKSPACE",
 }
 RING = 16
+# FP8 attention kernels (vitfp8_attn_varlen_kernel); "auto" lets the library pick.
+ATTN_KERNELS = {"auto": 0, "unit": 1, "persistent": 2, "two_tile": 3}
 E4M3_MAX = 448.0
 MAX_HEAD_DIM = 128
 
@@ -112,6 +114,10 @@ _ws_size = _sig("vitfp8_attn_workspace_size", ctypes.c_size_t, [_i32])
 _attn = _sig("vitfp8_attn_varlen", ctypes.c_int,
              [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
               ctypes.c_size_t, _vp])
+_attn_kernel = _sig("vitfp8_attn_varlen_kernel", ctypes.c_int,
+                    [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
+                     ctypes.c_size_t, _i32, _vp])
+_attn_kernel_for = _sig("vitfp8_attn_kernel_for", _i32, [_i32, _i32, _i32, _i32, _i32])
 _attn_noalloc = _sig("vitfp8_attn_varlen_noalloc", ctypes.c_int,
                      [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp])
 _attn_bf16 = _sig("vitfp8_attn_varlen_bf16", ctypes.c_int,
@@ -359,9 +365,17 @@ def selftest_bounded_wait(workspace, stream=None):
            "vitfp8_selftest_bounded_wait")
 
 
+def attn_kernel_for(num_seqs, max_seqlen, T, H, num_sms):
+    """Name of the kernel attn_varlen runs for these sizes on a GPU with num_sms SMs."""
+    k = _attn_kernel_for(int(num_seqs), int(max_seqlen), int(T), int(H), int(num_sms))
+    return {v: n for n, v in ATTN_KERNELS.items()}[k]
+
+
 def attn_varlen(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, out=None,
-                workspace=None, stream=None):
-    """FP8 varlen attention -> bf16 [T, H, D]."""
+                workspace=None, stream=None, kernel="auto"):
+    """FP8 varlen attention -> bf16 [T, H, D].
+
+    kernel: "auto" (the library's choice), "unit", "persistent" or "two_tile"."""
     nseq = _cu_info(cu_seqlens)
     T, H, D_pad = _check_codes(q8, k8, v8t)
     if sm_scale is None:
@@ -371,9 +385,17 @@ def attn_varlen(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, ou
     _need(out, torch.bfloat16, (T, H, D), "out")
     if workspace is None:
         workspace = Workspace(nseq, q8.device)
-    _check(_attn(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq, int(max_seqlen),
-                 int(T), int(H), int(D), int(D_pad), float(sm_scale), _ptr(out),
-                 _ptr(workspace.buf), workspace.nbytes, _stream(stream)), "vitfp8_attn_varlen")
+    if kernel not in ATTN_KERNELS:
+        raise ValueError("kernel must be one of %s" % sorted(ATTN_KERNELS))
+    if kernel == "auto":
+        _check(_attn(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq, int(max_seqlen),
+                     int(T), int(H), int(D), int(D_pad), float(sm_scale), _ptr(out),
+                     _ptr(workspace.buf), workspace.nbytes, _stream(stream)), "vitfp8_attn_varlen")
+    else:
+        _check(_attn_kernel(_ptr(q8), _ptr(k8), _ptr(v8t), state.ptr, _ptr(cu_seqlens), nseq,
+                            int(max_seqlen), int(T), int(H), int(D), int(D_pad), float(sm_scale),
+                            _ptr(out), _ptr(workspace.buf), workspace.nbytes, ATTN_KERNELS[kernel],
+                            _stream(stream)), "vitfp8_attn_varlen_kernel")
     return out
 
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvitfp8.so")
 LIB_CHECKED = os.path.join(PKG, "libvitfp8_checked.so")
-SOURCES = ["api.cu", "quant.cu", "attn_fp8.cu", "attn_bf16.cu", "attn_noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "quant.cu", "attn_fp8.cu", "attn_fp8_2tile.cu", "attn_bf16.cu", "attn_noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -183,14 +183,19 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs) {
     return ws_bytes(num_seqs);
 }
 
-vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
-                                 const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,
-                                 int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens,
-                                 int32_t H, int32_t D, int32_t D_pad, float sm_scale,
-                                 vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
-                                 cudaStream_t stream) {
+static_assert(VITFP8_ATTN_AUTO == kAttnAuto && VITFP8_ATTN_UNIT == kAttnUnit &&
+                  VITFP8_ATTN_PERSISTENT == kAttnPersistent && VITFP8_ATTN_TWO_TILE == kAttnTwoTile,
+              "kernel numbers of the header and the launcher agree");
+
+vitfp8_status vitfp8_attn_varlen_kernel(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                                        const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,
+                                        int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens,
+                                        int32_t H, int32_t D, int32_t D_pad, float sm_scale,
+                                        vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
+                                        int32_t kernel, cudaStream_t stream) {
     if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || H <= 0) return VITFP8_ERR_INVALID_ARG;
     if (D < 8 || (D & 7) || D_pad < D || (D_pad & 15)) return VITFP8_ERR_INVALID_ARG;
+    if (kernel < VITFP8_ATTN_AUTO || kernel > VITFP8_ATTN_TWO_TILE) return VITFP8_ERR_INVALID_ARG;
     if (D > VITFP8_MAX_HEAD_DIM || D_pad > VITFP8_MAX_HEAD_DIM) return VITFP8_ERR_UNSUPPORTED;
     if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f)) return VITFP8_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_tokens == 0) return VITFP8_OK;
@@ -202,7 +207,23 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
         return VITFP8_ERR_WORKSPACE;
     return launch_attn_fp8(q8, k8, v8t, d_state, d_cu_seqlens, num_seqs, max_seqlen, total_tokens, H, D, D_pad,
                            vitfp8_vt_stride(total_tokens), sm_scale,
-                           reinterpret_cast<uint16_t*>(out), d_workspace, stream);
+                           reinterpret_cast<uint16_t*>(out), d_workspace, kernel, stream);
+}
+
+vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                                 const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,
+                                 int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens,
+                                 int32_t H, int32_t D, int32_t D_pad, float sm_scale,
+                                 vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+    return vitfp8_attn_varlen_kernel(q8, k8, v8t, d_state, d_cu_seqlens, num_seqs, max_seqlen, total_tokens,
+                                     H, D, D_pad, sm_scale, out, d_workspace, workspace_bytes,
+                                     VITFP8_ATTN_AUTO, stream);
+}
+
+int32_t vitfp8_attn_kernel_for(int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens, int32_t H,
+                               int32_t num_sms) {
+    return attn_fp8_kernel_for(num_seqs, max_seqlen, total_tokens, H, num_sms);
 }
 
 vitfp8_status vitfp8_attn_varlen_bf16(const vitfp8_bf16* q, const vitfp8_bf16* k,

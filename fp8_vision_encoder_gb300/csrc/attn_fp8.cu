@@ -1377,13 +1377,6 @@ bool make_map_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
 // The kernels' dynamic shared memory (above the 48 KB default) is opted into
 // once per device: the attribute belongs to the current device.
 PerDeviceOnce g_smem_attr;
-
-// Longest segment for which the persistent kernel runs.  Its tiles cost about
-// 2 % more than those of the one-item-per-CTA kernel, and it saves most of a
-// work item's fixed cost (set-up, the first loads and scores): ahead for
-// segments of up to about 6000 tokens (3600 tokens: 7 %, 1024: 25 %, 256: 46 %),
-// behind from 8192 on (1 %).
-constexpr int kPersistentMaxSeqlen = 6144;
 }  // namespace
 
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
@@ -1400,23 +1393,24 @@ cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows
 vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
                               const vitfp8_scale_state* st, const int32_t* cu, int nseq, int max_seqlen,
                               int T, int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,
-                              void* ws, cudaStream_t s) {
+                              void* ws, int kernel, cudaStream_t s) {
     using namespace fa;
+    if (kernel < kAttnAuto || kernel > kAttnTwoTile) return VITFP8_ERR_INVALID_ARG;
     const int DV = (D + 15) & ~15;
-    CUtensorMap mq, mk, mv;
-    if (!make_map_3d_u8(&mq, q8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
-                        uint64_t(H) * Dp, 128, 1, BM) ||
-        !make_map_3d_u8(&mk, k8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
-                        uint64_t(H) * Dp, 128, 1, BN) ||
-        !make_map_3d_u8(&mv, v8t, uint64_t(Tv), uint64_t(Dp), uint64_t(H), uint64_t(Tv),
-                        uint64_t(Tv) * Dp, HALF, uint32_t(DV), 1))
-        return VITFP8_ERR_CUDA;
-
     int dev = -1, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return VITFP8_ERR_CUDA;
-    if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, nsm, BN, ws, s) != cudaSuccess)
+    if (kernel == kAttnAuto) kernel = attn_fp8_kernel_for(nseq, max_seqlen, T, H, nsm);
+    // Q boxes of 128 rows and V^T boxes of 128 keys for every kernel; K boxes
+    // of one key tile (256 keys, 128 for the two-tile kernel).
+    CUtensorMap mq, mk, mv;
+    if (!make_map_3d_u8(&mq, q8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
+                        uint64_t(H) * Dp, 128, 1, BM) ||
+        !make_map_3d_u8(&mk, k8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
+                        uint64_t(H) * Dp, 128, 1, kernel == kAttnTwoTile ? 128u : uint32_t(BN)) ||
+        !make_map_3d_u8(&mv, v8t, uint64_t(Tv), uint64_t(Dp), uint64_t(H), uint64_t(Tv),
+                        uint64_t(Tv) * Dp, HALF, uint32_t(DV), 1))
         return VITFP8_ERR_CUDA;
 
     if (!g_smem_attr.run(dev, [] {
@@ -1444,16 +1438,17 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     prm.KS = (D + 31) / 32;
     prm.sm_scale = sm_scale;
     prm.out_elems = int64_t(T) * H * D;
+    if (kernel == kAttnTwoTile) return launch_attn_fp8_2tile(mq, mk, mv, prm, nsm, s);
+
+    if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, nsm, BN, ws, s) != cudaSuccess)
+        return VITFP8_ERR_CUDA;
     // Units (work items, or parts of split items) are at most
     // (T / 128 + nseq) * H + kSplitMaxParts; CTAs without a unit return at once.
     const long long max_units = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H + kSplitMaxParts;
     if (max_units > 0x7FFFFFFFLL) return VITFP8_ERR_UNSUPPORTED;
-    // Work items are at most (T / 128 + nseq) * H; with no more than one wave
-    // of them there is no next unit to overlap.
-    const long long max_items = (long long)((T + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM + nseq) * H;
-    if (max_seqlen <= kPersistentMaxSeqlen && max_items > nsm) {
-        // Short segments: one CTA per SM walking the units, so a unit's set-up
-        // and first loads overlap the previous unit's last tiles.
+    if (kernel == kAttnPersistent) {
+        // One CTA per SM walking the units, so a unit's set-up and first loads
+        // overlap the previous unit's last tiles (worth it for short segments).
         const unsigned grid = unsigned(max_units < nsm ? max_units : nsm);
         attn_fp8_persistent_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);
     } else {

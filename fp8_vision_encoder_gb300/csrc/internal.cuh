@@ -84,12 +84,47 @@ cudaError_t launch_selftest_bounds(void* ws, cudaStream_t s);
 // split_bn keys) of the last wave's items over up to nsm CTAs.
 cudaError_t launch_attn_plan(const int32_t* cu, int nseq, int T, int H, int rows_per_item,
                              int nsm, int split_bn, void* ws, cudaStream_t s);
-// max_seqlen (>= every segment's length) picks the kernel: persistent for
-// short segments, one work item per CTA otherwise (same results).
+// FP8 attention kernels (the values of vitfp8_attn_kernel in vitfp8.h).
+constexpr int kAttnAuto = 0;        // attn_fp8_kernel_for() picks
+constexpr int kAttnUnit = 1;        // one CTA per 128-row work item (attn_fp8.cu)
+constexpr int kAttnPersistent = 2;  // one CTA per SM walking the work items (attn_fp8.cu)
+constexpr int kAttnTwoTile = 3;     // one CTA per 256-row unit, two query tiles (attn_fp8_2tile.cu)
+// Two-tile kernel: longest segment at least this long, at least kTwoTileMinWaves
+// waves of 256-row units, and the last wave's shortfall at most
+// kTwoTileMaxTail of the time (ceil(w) / w <= 1 + kTwoTileMaxTail).
+constexpr int kTwoTileMinSeqlen = 2048;
+constexpr double kTwoTileMinWaves = 2.0;
+constexpr double kTwoTileMaxTail = 0.12;
+// Persistent kernel: longest segment at most this long and more than one wave of items.
+constexpr int kPersistentMaxSeqlen = 6144;
+
+// The kernel the FP8 attention call runs when none is asked for, from what
+// the host knows: segment count, the bound on segment lengths, token count,
+// heads and SM count.  The two-tile kernel's units are estimated as
+// H * (T + 128 * nseq) / 256 (a segment's last unit is half full on average).
+inline int attn_fp8_kernel_for(int nseq, int max_seqlen, int T, int H, int nsm) {
+    if (nsm <= 0 || nseq <= 0 || T <= 0 || H <= 0) return kAttnUnit;
+    if (max_seqlen >= kTwoTileMinSeqlen) {
+        const double waves = double(H) * (double(T) + 128.0 * nseq) / 256.0 / double(nsm);
+        if (waves >= kTwoTileMinWaves) {
+            double full = double(int64_t(waves));
+            if (full < waves) full += 1.0;
+            if (full <= waves * (1.0 + kTwoTileMaxTail)) return kAttnTwoTile;
+        }
+    }
+    const long long max_items = (long long)((T + 127) / 128 + nseq) * H;
+    if (max_seqlen <= kPersistentMaxSeqlen && max_items > nsm) return kAttnPersistent;
+    return kAttnUnit;
+}
+
+// kernel: one of the kAttn* values (kAttnAuto: attn_fp8_kernel_for).  All
+// kernels compute the same attention; the unit and persistent kernels give
+// the same bits, the two-tile kernel can differ in the last bit of about 1 %
+// of the outputs (its reference moves at 128-key boundaries).
 vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
                               const vitfp8_scale_state* st, const int32_t* cu, int nseq, int max_seqlen,
                               int T, int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,
-                              void* ws, cudaStream_t s);
+                              void* ws, int kernel, cudaStream_t s);
 
 // ---- launcher (attn_bf16.cu)
 vitfp8_status launch_attn_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,

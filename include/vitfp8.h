@@ -253,14 +253,20 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs);
  *          word and the partial results of a key-range split.  Calls sharing
  *          one workspace must be stream-ordered.
  *
- * Scheduling: one work unit per 128-query tile of a (segment, head).  When
- * the tiles leave a last wave that fills at most half the GPU, the key range
- * of each of those tiles is split over up to 4 units, and the unit that
- * finishes last combines the parts by exact powers of two (same numerics up
- * to the fp32 summation order); the result is deterministic for a given input
- * and GPU.  With max_seqlen <= 6144 and more than one wave of work items a
- * persistent kernel (one CTA per SM) runs the units, otherwise one CTA per
- * unit; both give the same bits, so max_seqlen affects only the speed.
+ * Scheduling (vitfp8_attn_kernel_for picks one of three kernels; all compute
+ * the attention above):
+ *  - VITFP8_ATTN_UNIT: one CTA per 128-query tile of a (segment, head).  When
+ *    the tiles leave a last wave that fills at most half the GPU, the key range
+ *    of each of those tiles is split over up to 4 units, and the unit that
+ *    finishes last combines the parts by exact powers of two (same numerics up
+ *    to the fp32 summation order).
+ *  - VITFP8_ATTN_PERSISTENT: the same units run by one CTA per SM (for short
+ *    segments); the same bits as VITFP8_ATTN_UNIT.
+ *  - VITFP8_ATTN_TWO_TILE: one CTA per 256-query unit (two 128-row tiles
+ *    sharing each key tile), for long segments whose units fill the GPU's
+ *    waves well.  Its reference moves at 128-key boundaries, so about 1 % of
+ *    the outputs can differ from the other kernels' in the last bf16 bit.
+ * The result is deterministic for a given input, max_seqlen and GPU.
  */
 vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
                                  const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,
@@ -268,6 +274,39 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
                                  int32_t H, int32_t D, int32_t D_pad, float sm_scale,
                                  vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
+
+/* FP8 attention kernels (vitfp8_attn_varlen_kernel's `kernel`). */
+#define VITFP8_ATTN_AUTO 0       /* vitfp8_attn_kernel_for decides */
+#define VITFP8_ATTN_UNIT 1       /* one CTA per 128-query work item */
+#define VITFP8_ATTN_PERSISTENT 2 /* one CTA per SM walking the work items */
+#define VITFP8_ATTN_TWO_TILE 3   /* one CTA per 256-query unit */
+
+/*
+ * vitfp8_attn_varlen with the kernel named by `kernel` (one of the
+ * VITFP8_ATTN_* values; VITFP8_ATTN_AUTO is vitfp8_attn_varlen itself).
+ * Every kernel takes every valid input; the choice only changes speed and,
+ * for VITFP8_ATTN_TWO_TILE, the last bit of some outputs.  Errors as for
+ * vitfp8_attn_varlen, plus VITFP8_ERR_INVALID_ARG for an unknown kernel.
+ */
+vitfp8_status vitfp8_attn_varlen_kernel(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                                        const vitfp8_scale_state* d_state, const int32_t* d_cu_seqlens,
+                                        int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens,
+                                        int32_t H, int32_t D, int32_t D_pad, float sm_scale,
+                                        vitfp8_bf16* out, void* d_workspace, size_t workspace_bytes,
+                                        int32_t kernel, cudaStream_t stream);
+
+/*
+ * The kernel vitfp8_attn_varlen runs for these sizes on a GPU with num_sms
+ * SMs (host only, no device call):
+ *  - VITFP8_ATTN_TWO_TILE when max_seqlen >= 2048 and the estimated 256-query
+ *    units, w = H (T + 128 num_seqs) / 256 / num_sms waves, are at least two
+ *    waves with ceil(w) / w <= 1.12 (the last wave nearly full);
+ *  - else VITFP8_ATTN_PERSISTENT when max_seqlen <= 6144 and the 128-query
+ *    items, (ceil(T / 128) + num_seqs) H, are more than num_sms;
+ *  - else VITFP8_ATTN_UNIT (also for non-positive sizes).
+ */
+int32_t vitfp8_attn_kernel_for(int32_t num_seqs, int32_t max_seqlen, int32_t total_tokens, int32_t H,
+                               int32_t num_sms);
 
 /*
  * BF16 variable-length non-causal attention, the comparison path of

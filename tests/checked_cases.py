@@ -33,7 +33,7 @@ def _cu(seqlens):
     return torch.tensor(cu, dtype=torch.int32, device="cuda")
 
 
-def _case(vf, name, seqlens, H, D, seed, dynamic=True, layout="packed"):
+def _case(vf, name, seqlens, H, D, seed, dynamic=True, layout="packed", kernel="auto"):
     T = sum(seqlens)
     Dp = vf.default_d_pad(D)
     Tv = vf.vt_stride(T)
@@ -65,7 +65,7 @@ def _case(vf, name, seqlens, H, D, seed, dynamic=True, layout="packed"):
     ws = vf.Workspace(len(seqlens))
     bo, o = _guarded(T * H * D * 2)
     o = o.view(torch.bfloat16).view(T, H, D)
-    vf.attn_varlen(q8, k8, v8t, st, cu, max(seqlens), D, out=o, workspace=ws)
+    vf.attn_varlen(q8, k8, v8t, st, cu, max(seqlens), D, out=o, workspace=ws, kernel=kernel)
     ws16 = vf.Workspace(len(seqlens))
     bo16, o16 = _guarded(T * H * D * 2)
     o16 = o16.view(torch.bfloat16).view(T, H, D)
@@ -91,6 +91,10 @@ def run_cases(vf):
         ("split", [2048, 600], 2, 128, 45, True, "packed"),   # every item's key range split
         ("long", [7000, 300], 1, 128, 46, True, "packed"),    # one CTA per work item (segments > 6144)
         ("psplit", [2048], 12, 128, 47, True, "packed"),      # persistent kernel, last wave split
+        # two-tile kernel: one S buffer (d = 128), one per tile (d = 80, 40)
+        ("tt128", [300, 1000, 129, 1], 2, 128, 48, True, "packed", "two_tile"),
+        ("tt80", [600, 77, 256], 3, 80, 49, True, "padded", "two_tile"),
+        ("tt40", [3, 130, 61, 700], 2, 40, 50, True, "packed", "two_tile"),
     ]
     for D in range(8, 129, 8):
         cases.append(("d%d" % D, [3, 130, 61], 2, D, 100 + D, D % 16 == 0, "packed"))

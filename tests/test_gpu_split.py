@@ -39,7 +39,7 @@ def nsm():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def _run(vf, seqlens, H, D, seed, outliers=True):
+def _run(vf, seqlens, H, D, seed, outliers=True, kernel="unit"):
     cu, cul = cu_tensor(seqlens)
     st = vf.ScaleState().init()
     ost = oscales.ScaleState()
@@ -49,7 +49,7 @@ def _run(vf, seqlens, H, D, seed, outliers=True):
     oracle_push(ost, q, k, v)
     q8, k8, v8t = vf.quantize_unpad(st, q, k, v, cu)
     ws = vf.Workspace(len(seqlens))
-    out = vf.attn_varlen(q8, k8, v8t, st, cu, max(seqlens), D, workspace=ws)
+    out = vf.attn_varlen(q8, k8, v8t, st, cu, max(seqlens), D, workspace=ws, kernel=kernel)
     torch.cuda.synchronize()
     assert ws.error() == 0
     hdr = ws.buf[:20].view(torch.int32).cpu().tolist()   # error, items, nseq, split_first, split_k
@@ -102,7 +102,7 @@ def test_split_ragged_and_deterministic(vf):
     for _ in range(3):
         ws = vf.Workspace(len(seqlens))
         outs.append(vf.attn_varlen(r1["q8"], r1["k8"], r1["v8t"], r1["st"], r1["cu_t"], max(seqlens), D,
-                                   workspace=ws))
+                                   workspace=ws, kernel="unit"))
     torch.cuda.synchronize()
     for o in outs:
         assert torch.equal(o.view(torch.int16), r1["out"].view(torch.int16))
