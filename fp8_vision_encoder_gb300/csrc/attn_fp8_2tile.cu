@@ -11,9 +11,10 @@
 //   A work unit is 256 consecutive queries of one (segment, head): query tiles
 //   A (rows 0..127) and B (rows 128..255), against every 128-key tile of the
 //   segment.  Each softmax thread owns one query row (TMEM access shape
-//   32x32b): warps 0-3 rows of tile A, warps 4-7 rows of tile B, so every
-//   scheduler holds one warp of each tile.  The K and V tiles a unit loads
-//   serve 256 queries, and a segment has half as many units as 128-row items.
+//   32x32b; the row's 128 scores and their maximum come in one load): warps
+//   0-3 rows of tile A, warps 4-7 rows of tile B, so every scheduler holds
+//   one warp of each tile.  The K and V tiles a unit loads serve 256
+//   queries, and a segment has half as many units as 128-row items.
 //
 //   Up to d = 128 the two tiles share one 128-column S buffer in TMEM:
 //   S_A(j), S_B(j), S_A(j+1), ... each wait for the other tile's softmax to
@@ -24,7 +25,7 @@
 //   softmax works on the current ones.
 //
 //   warp 8      TMA: Q_A and Q_B once, then K tiles (128 keys x 128 bytes) and
-//               V^T tiles (d rows x 128 keys) through a 5-stage ring.
+//               V^T tiles (d rows x 128 keys) through a 4-stage ring.
 //   warp 9      S issuer (one thread): S_X(j) = Q_X K_j^T, 128 x 128 per tile.
 //   warp 10     P.V issuer (one thread): O_X += P_X(j) V_j, alternating A, B.
 //   warp 11     idle (completes the producer warpgroup of the register split).
@@ -74,7 +75,7 @@ __device__ __forceinline__ void named_bar_sync() {
 
 constexpr int BM = 128;                  // rows per query tile
 constexpr int BN = 128;                  // keys per key tile
-constexpr int NST = 5;                   // K/V ring stages
+constexpr int NST = 4;                   // K/V ring stages
 constexpr int NUM_THREADS = 384;
 // setmaxnreg split: 8 softmax warps x 176 + 4 producer warps x 152 registers
 // = 64 512, the launch's 384 threads x 168.
@@ -392,17 +393,16 @@ attn_fp8_2tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             const uint32_t par = uint32_t(j) & 1u;
             if (!(ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + g), par, abort_flag, err)))) break;
             tc_fence_after();
-            // 128 scores of this row, with each 32-key chunk's maximum.
+            // 128 scores of this row and their maximum.
             float sf[128];
-            float mq[4];
-            tmem_ld32_s128_max(tS, sf, mq);
+            float pmax;
+            tmem_ld32_x128_max(tS, sf, pmax);
             // S is in registers: the tensor core may overwrite it.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SFREE + g));
 
             const int key0 = kb0 + j * BN;
-            float pmax = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             if (key0 < seg_s || key0 + BN > seg_e) {
                 // First or last tile: keys outside the segment are masked and
                 // the maximum is taken over the keys left.
@@ -435,6 +435,14 @@ attn_fp8_2tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 m_ref = mnew;
                 need = true;
             }
+            if (j > 0) {
+                // The tile's previous P.V is complete (P's columns are free, O
+                // with l is final up to that key tile).  Waited for before the
+                // exponentials: that product was issued a whole tile ago, and
+                // the P store then follows the exponentials without a wait.
+                if (!(ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL + g), par ^ 1u, abort_flag, err)))) break;
+                tc_fence_after();
+            }
             const float bias = PSHIFT - m_ref;
             const uint64_t b2 = f32x2_pack(bias, bias);
             // P' = E4M3(2^(x - m_ref + 8)), four keys per 32-bit word.
@@ -445,12 +453,6 @@ attn_fp8_2tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 f32x2_unpack(ffma2(f32x2_pack(sf[4 * q], sf[4 * q + 1]), c2, b2), y0, y1);
                 f32x2_unpack(ffma2(f32x2_pack(sf[4 * q + 2], sf[4 * q + 3]), c2, b2), y2, y3);
                 pk[q] = cvt_e4m3x4(ex2_approx(y0), ex2_approx(y1), ex2_approx(y2), ex2_approx(y3));
-            }
-            if (j > 0) {
-                // The tile's previous P.V is complete: P's columns are free and
-                // O (with l) is final up to that key tile.
-                if (!(ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL + g), par ^ 1u, abort_flag, err)))) break;
-                tc_fence_after();
             }
             tmem_st32_x32_sync(tP, pk);
             if (__any_sync(0xFFFFFFFFu, need)) rescale_o(tO, nco, oscale);
