@@ -322,7 +322,7 @@ __device__ __noinline__ void split_part_epilogue(const SplitOut so, uint32_t tO,
 }
 
 // Softmax of one key tile, shared by both kernels (the 8 softmax warps, two
-// threads per row): wait for S, read it with its 32-key chunk maxima, mask
+// threads per row): wait for S, read it with its maximum, mask
 // keys outside the segment (first and last tile only), move the row's
 // reference when the tile's maximum passes it (O and l rescaled by an exact
 // power of two), write P' = E4M3(2^(x - m_ref + 8)) and signal P.V.  gpar is
@@ -345,16 +345,15 @@ __device__ __forceinline__ bool softmax_tile(const SoftmaxWarp& x, int key0, int
     auto BAR = [&](int i) -> uint32_t { return x.bar0 + 8u * uint32_t(i); };
     if (!__all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL), gpar, x.abort_flag, x.err))) return false;
     tc_fence_after();
-    // The loads also return each 32-key chunk's maximum (tcgen05.ld.red).
+    // One load returns the 128 scores and their maximum (tcgen05.ld.red).
     float sf[128];
-    float mq[4];
-    tmem_ld_s128_max<HALF>(x.tS, sf, mq);
+    float pmax;
+    tmem_ld_s128_max<HALF>(x.tS, sf, pmax);
     // S is in registers: the tensor core may overwrite it with the next S.
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(BAR(B_SFREE));
 
-    float pmax = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
     if (key0 < seg_s || key0 + HALF > seg_e) {
         // First or last tile: keys outside the segment are masked, and
         // the maximum is taken over the keys left.
