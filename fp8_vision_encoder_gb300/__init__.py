@@ -42,7 +42,7 @@ STATUS_NAMES = {
 }
 RING = 16
 # FP8 attention kernels (vitfp8_attn_varlen_kernel); "auto" lets the library pick.
-ATTN_KERNELS = {"auto": 0, "unit": 1, "persistent": 2, "two_tile": 3}
+ATTN_KERNELS = {"auto": 0, "unit": 1, "persistent": 2, "two_tile": 3, "two_tile_persistent": 4}
 E4M3_MAX = 448.0
 MAX_HEAD_DIM = 128
 

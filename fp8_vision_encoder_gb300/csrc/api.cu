@@ -184,7 +184,8 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs) {
 }
 
 static_assert(VITFP8_ATTN_AUTO == kAttnAuto && VITFP8_ATTN_UNIT == kAttnUnit &&
-                  VITFP8_ATTN_PERSISTENT == kAttnPersistent && VITFP8_ATTN_TWO_TILE == kAttnTwoTile,
+                  VITFP8_ATTN_PERSISTENT == kAttnPersistent && VITFP8_ATTN_TWO_TILE == kAttnTwoTile &&
+                  VITFP8_ATTN_TWO_TILE_PERSISTENT == kAttnTwoTilePersistent,
               "kernel numbers of the header and the launcher agree");
 
 vitfp8_status vitfp8_attn_varlen_kernel(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
@@ -195,7 +196,7 @@ vitfp8_status vitfp8_attn_varlen_kernel(const uint8_t* q8, const uint8_t* k8, co
                                         int32_t kernel, cudaStream_t stream) {
     if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || H <= 0) return VITFP8_ERR_INVALID_ARG;
     if (D < 8 || (D & 7) || D_pad < D || (D_pad & 15)) return VITFP8_ERR_INVALID_ARG;
-    if (kernel < VITFP8_ATTN_AUTO || kernel > VITFP8_ATTN_TWO_TILE) return VITFP8_ERR_INVALID_ARG;
+    if (kernel < VITFP8_ATTN_AUTO || kernel > VITFP8_ATTN_TWO_TILE_PERSISTENT) return VITFP8_ERR_INVALID_ARG;
     if (D > VITFP8_MAX_HEAD_DIM || D_pad > VITFP8_MAX_HEAD_DIM) return VITFP8_ERR_UNSUPPORTED;
     if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f)) return VITFP8_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_tokens == 0) return VITFP8_OK;

@@ -25,10 +25,11 @@ struct AttnParams {
     int64_t out_elems;  // T * H * D (checked build)
 };
 
-// The two-tile FP8 kernel (attn_fp8_2tile.cu): plans 256-row units and
-// launches; the tensor maps are attn_fp8.cu's with a 128-key K box.
+// The two-tile FP8 kernels (attn_fp8_2tile.cu): plan 256-row units and
+// launch one CTA per unit or (persistent) one CTA per SM; the tensor maps are
+// attn_fp8.cu's with a 128-key K box.
 vitfp8_status launch_attn_fp8_2tile(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                    const AttnParams& prm, int nsm, cudaStream_t s);
+                                    const AttnParams& prm, int nsm, bool persistent, cudaStream_t s);
 
 // Work item -> the record of its segment (the last record whose first_item
 // is <= item).  In two steps so that a caller can issue every load it needs

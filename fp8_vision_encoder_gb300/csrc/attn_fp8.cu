@@ -1394,7 +1394,7 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
                               int T, int H, int D, int Dp, int64_t Tv, float sm_scale, uint16_t* out,
                               void* ws, int kernel, cudaStream_t s) {
     using namespace fa;
-    if (kernel < kAttnAuto || kernel > kAttnTwoTile) return VITFP8_ERR_INVALID_ARG;
+    if (kernel < kAttnAuto || kernel > kAttnTwoTilePersistent) return VITFP8_ERR_INVALID_ARG;
     const int DV = (D + 15) & ~15;
     int dev = -1, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1407,7 +1407,7 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     if (!make_map_3d_u8(&mq, q8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
                         uint64_t(H) * Dp, 128, 1, BM) ||
         !make_map_3d_u8(&mk, k8, uint64_t(Dp), uint64_t(H), uint64_t(T), uint64_t(Dp),
-                        uint64_t(H) * Dp, 128, 1, kernel == kAttnTwoTile ? 128u : uint32_t(BN)) ||
+                        uint64_t(H) * Dp, 128, 1, kernel >= kAttnTwoTile ? 128u : uint32_t(BN)) ||
         !make_map_3d_u8(&mv, v8t, uint64_t(Tv), uint64_t(Dp), uint64_t(H), uint64_t(Tv),
                         uint64_t(Tv) * Dp, HALF, uint32_t(DV), 1))
         return VITFP8_ERR_CUDA;
@@ -1437,7 +1437,8 @@ vitfp8_status launch_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_
     prm.KS = (D + 31) / 32;
     prm.sm_scale = sm_scale;
     prm.out_elems = int64_t(T) * H * D;
-    if (kernel == kAttnTwoTile) return launch_attn_fp8_2tile(mq, mk, mv, prm, nsm, s);
+    if (kernel >= kAttnTwoTile)
+        return launch_attn_fp8_2tile(mq, mk, mv, prm, nsm, kernel == kAttnTwoTilePersistent, s);
 
     if (launch_attn_plan(cu, nseq, T, H, ROWS_PER_ITEM, nsm, BN, ws, s) != cudaSuccess)
         return VITFP8_ERR_CUDA;

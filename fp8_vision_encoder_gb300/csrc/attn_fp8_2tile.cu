@@ -104,10 +104,19 @@ constexpr int B_SFREE = B_SFULL + 2;       // [2]: that S read by the tile's 4 s
 constexpr int B_PFULL = B_SFREE + 2;       // [2]: P written by the tile's 4 softmax warps
 constexpr int B_OFULL = B_PFULL + 2;       // [2]: the tile's P.V (and every earlier one) complete
 constexpr int B_FINAL = B_OFULL + 2;
-constexpr int NBAR = B_FINAL + 1;
+// Persistent kernel only:
+constexpr int B_QEMPTY = B_FINAL + 1;      // every S product of the current unit is done with Q
+constexpr int B_OFREE = B_QEMPTY + 1;      // [2]: the tile's 4 softmax warps have read the unit's O
+constexpr int B_IFULL = B_OFREE + 2;       // [2]: unit description written
+constexpr int B_IEMPTY = B_IFULL + 2;      // [2]: description used up by all 10 consumers
+constexpr int NBAR = B_IEMPTY + 2;
+constexpr int IEMPTY_COUNT = 10;           // S issuer, P.V issuer, 8 softmax warps
 constexpr int SM_TMEMPTR = SM_BAR + NBAR * 8;
 constexpr int SM_ABORT = SM_TMEMPTR + 4;
-constexpr int SM_USED = SM_ABORT + 4;
+constexpr int SM_INFO = SM_ABORT + 4;      // persistent: 2 unit descriptions of INFO_INTS ints
+constexpr int INFO_INTS = 8;
+constexpr int I_WORK = 0, I_H = 1, I_Q0 = 2, I_SEGS = 3, I_SEGE = 4, I_KB0 = 5, I_NKV = 6;
+constexpr int SM_USED = SM_INFO + 2 * INFO_INTS * 4;
 constexpr int SMEM_BYTES = SM_USED + 1024;  // + slack to align the base to 1024
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 512;
@@ -155,6 +164,125 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, int nc, float s) {
         tmem_ld32_x16(tO + uint32_t(c), o);
         scale_words(o, s2);
         tmem_st32_x16_sync(tO + uint32_t(c), o);
+    }
+}
+
+// Softmax of one key tile by one warp of query tile x.g (one thread per row),
+// shared by both kernels: wait for the scores, read them with their maximum,
+// mask keys outside the segment (first and last tile only), move the row's
+// reference when the tile's maximum passes it, wait for the tile's previous
+// P.V, write P' = E4M3(2^(x - m_ref + 8)), rescale O and l by the exact power
+// of two when the reference moved, and hand P to the P.V issuer.  par is the
+// key tile's barrier parity; first marks a unit's first tile (whose P.V wait
+// the previous unit's epilogue already did).  False when a wait gave up.
+struct Tile2 {
+    uint32_t tS, tO, tP;      // this warp's TMEM lanes of S, O and P
+    uint32_t bar0;            // shared-memory address of barrier 0
+    uint64_t c2;              // (c, c)
+    float c;                  // log2 units per raw score
+    int nco;                  // O columns: d + 16
+    int g;                    // query tile: 0 = A, 1 = B
+    volatile int* abort_flag;
+    int32_t* err;
+};
+
+__device__ __forceinline__ bool softmax_tile2(const Tile2& x, int key0, int seg_s, int seg_e, bool first,
+                                              uint32_t par, float& m_ref) {
+    const int lane = threadIdx.x & 31;
+    auto BAR = [&](int i) -> uint32_t { return x.bar0 + 8u * uint32_t(i); };
+    if (!__all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + x.g), par, x.abort_flag, x.err))) return false;
+    tc_fence_after();
+    // 128 scores of this row and their maximum.
+    float sf[128];
+    float pmax;
+    tmem_ld32_x128_max(x.tS, sf, pmax);
+    // S is in registers: the tensor core may overwrite it.
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(BAR(B_SFREE + x.g));
+
+    if (key0 < seg_s || key0 + BN > seg_e) {
+        // First or last tile: keys outside the segment are masked and
+        // the maximum is taken over the keys left.
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+            const int key = key0 + i;
+            if ((key < seg_s || key >= seg_e) && VF_IN(i, 1, 128, x.err)) sf[i] = -INFINITY;
+        }
+        float mx0 = fmaxf(sf[0], sf[1]), mx1 = fmaxf(sf[2], sf[3]);
+        float mx2 = fmaxf(sf[4], sf[5]), mx3 = fmaxf(sf[6], sf[7]);
+#pragma unroll
+        for (int i = 8; i < 128; i += 8) {
+            mx0 = fmax3(mx0, sf[i], sf[i + 1]);
+            mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
+            mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
+            mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
+        }
+        pmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+    }
+    // Move the reference only when the tile's maximum passes it by
+    // more than SLACK; then O and l are rescaled by an exact power of two.
+    const float xmax = pmax * x.c;
+    float oscale = 1.0f;
+    bool need = false;
+    if (first) {
+        m_ref = ceilf(xmax);
+    } else if (xmax > m_ref + SLACK) {
+        const float mnew = ceilf(xmax);
+        oscale = exp2_int(m_ref - mnew);
+        m_ref = mnew;
+        need = true;
+    }
+    if (!first) {
+        // The tile's previous P.V is complete (P's columns are free, O
+        // with l is final up to that key tile).  Waited for before the
+        // exponentials: that product was issued a whole tile ago, and
+        // the P store then follows the exponentials without a wait.
+        if (!__all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL + x.g), par ^ 1u, x.abort_flag, x.err))) return false;
+        tc_fence_after();
+    }
+    const float bias = PSHIFT - m_ref;
+    const uint64_t b2 = f32x2_pack(bias, bias);
+    // P' = E4M3(2^(x - m_ref + 8)), four keys per 32-bit word.
+    uint32_t pk[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+        float y0, y1, y2, y3;
+        f32x2_unpack(ffma2(f32x2_pack(sf[4 * q], sf[4 * q + 1]), x.c2, b2), y0, y1);
+        f32x2_unpack(ffma2(f32x2_pack(sf[4 * q + 2], sf[4 * q + 3]), x.c2, b2), y2, y3);
+        pk[q] = cvt_e4m3x4(ex2_approx(y0), ex2_approx(y1), ex2_approx(y2), ex2_approx(y3));
+    }
+    tmem_st32_x32_sync(x.tP, pk);
+    if (__any_sync(0xFFFFFFFFu, need)) rescale_o(x.tO, x.nco, oscale);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(BAR(B_PFULL + x.g));
+    return true;
+}
+
+// Epilogue of one query row (its thread): o = O * scale_v / l (l = O's column
+// DV), rounded to bf16, 16 columns at a time; stored only for rows inside the
+// segment.  row0 is the row's first output element.
+__device__ __forceinline__ void store_row2(uint32_t tO, const AttnParams& p, float scale_v, int64_t row0,
+                                           bool row_valid, int32_t* err) {
+    [[maybe_unused]] int32_t* e = err;   // checked build only
+    const float l = __uint_as_float(tmem_ld32_x1(tO + uint32_t(p.DV)));
+    const float os = scale_v / l;
+    uint16_t* orow = p.out + row0;
+    for (int c0 = 0; c0 < p.DV; c0 += 16) {
+        uint32_t o[16];
+        tmem_ld32_x16(tO + uint32_t(c0), o);
+        if (!row_valid) continue;
+#pragma unroll
+        for (int q = 0; q < 16; q += 8) {
+            if (c0 + q + 8 > p.D || !VF_IN(row0 + c0 + q, 8, p.out_elems, e)) continue;
+            uint4 v;
+            v.x = cvt_bf16x2(__uint_as_float(o[q]) * os, __uint_as_float(o[q + 1]) * os);
+            v.y = cvt_bf16x2(__uint_as_float(o[q + 2]) * os, __uint_as_float(o[q + 3]) * os);
+            v.z = cvt_bf16x2(__uint_as_float(o[q + 4]) * os, __uint_as_float(o[q + 5]) * os);
+            v.w = cvt_bf16x2(__uint_as_float(o[q + 6]) * os, __uint_as_float(o[q + 7]) * os);
+            *reinterpret_cast<uint4*>(orow + c0 + q) = v;
+        }
     }
 }
 
@@ -389,99 +517,380 @@ attn_fp8_2tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         const int nco = p.DV + 16;
         float m_ref = 0.0f;
         bool ok = true;
+        const Tile2 tx{tS, tO, tP, sb + SM_BAR, c2, c, nco, g, abort_flag, err};
         for (int j = 0; j < nkv; ++j) {
-            const uint32_t par = uint32_t(j) & 1u;
-            if (!(ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_SFULL + g), par, abort_flag, err)))) break;
-            tc_fence_after();
-            // 128 scores of this row and their maximum.
-            float sf[128];
-            float pmax;
-            tmem_ld32_x128_max(tS, sf, pmax);
-            // S is in registers: the tensor core may overwrite it.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_SFREE + g));
-
-            const int key0 = kb0 + j * BN;
-            if (key0 < seg_s || key0 + BN > seg_e) {
-                // First or last tile: keys outside the segment are masked and
-                // the maximum is taken over the keys left.
-#pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    const int key = key0 + i;
-                    if ((key < seg_s || key >= seg_e) && VF_IN(i, 1, 128, err)) sf[i] = -INFINITY;
-                }
-                float mx0 = fmaxf(sf[0], sf[1]), mx1 = fmaxf(sf[2], sf[3]);
-                float mx2 = fmaxf(sf[4], sf[5]), mx3 = fmaxf(sf[6], sf[7]);
-#pragma unroll
-                for (int i = 8; i < 128; i += 8) {
-                    mx0 = fmax3(mx0, sf[i], sf[i + 1]);
-                    mx1 = fmax3(mx1, sf[i + 2], sf[i + 3]);
-                    mx2 = fmax3(mx2, sf[i + 4], sf[i + 5]);
-                    mx3 = fmax3(mx3, sf[i + 6], sf[i + 7]);
-                }
-                pmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-            }
-            // Move the reference only when the tile's maximum passes it by
-            // more than SLACK; then O and l are rescaled by an exact power of two.
-            const float xmax = pmax * c;
-            float oscale = 1.0f;
-            bool need = false;
-            if (j == 0) {
-                m_ref = ceilf(xmax);
-            } else if (xmax > m_ref + SLACK) {
-                const float mnew = ceilf(xmax);
-                oscale = exp2_int(m_ref - mnew);
-                m_ref = mnew;
-                need = true;
-            }
-            if (j > 0) {
-                // The tile's previous P.V is complete (P's columns are free, O
-                // with l is final up to that key tile).  Waited for before the
-                // exponentials: that product was issued a whole tile ago, and
-                // the P store then follows the exponentials without a wait.
-                if (!(ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL + g), par ^ 1u, abort_flag, err)))) break;
-                tc_fence_after();
-            }
-            const float bias = PSHIFT - m_ref;
-            const uint64_t b2 = f32x2_pack(bias, bias);
-            // P' = E4M3(2^(x - m_ref + 8)), four keys per 32-bit word.
-            uint32_t pk[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                float y0, y1, y2, y3;
-                f32x2_unpack(ffma2(f32x2_pack(sf[4 * q], sf[4 * q + 1]), c2, b2), y0, y1);
-                f32x2_unpack(ffma2(f32x2_pack(sf[4 * q + 2], sf[4 * q + 3]), c2, b2), y2, y3);
-                pk[q] = cvt_e4m3x4(ex2_approx(y0), ex2_approx(y1), ex2_approx(y2), ex2_approx(y3));
-            }
-            tmem_st32_x32_sync(tP, pk);
-            if (__any_sync(0xFFFFFFFFu, need)) rescale_o(tO, nco, oscale);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PFULL + g));
+            ok = softmax_tile2(tx, kb0 + j * BN, seg_s, seg_e, j == 0, uint32_t(j) & 1u, m_ref);
+            if (!ok) break;
         }
         if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL + g), uint32_t(nkv - 1) & 1u, abort_flag, err));
         if (ok) {
-            // o = O * scale_v / l (l = column DV), rounded to bf16, 16 columns at a time.
             tc_fence_after();
-            const float l = __uint_as_float(tmem_ld32_x1(tO + uint32_t(p.DV)));
-            const float os = scale_v / l;
-            const int64_t row0 = (int64_t(qrow) * p.H + h) * p.D;
-            uint16_t* orow = p.out + row0;
-            for (int c0 = 0; c0 < p.DV; c0 += 16) {
-                uint32_t o[16];
-                tmem_ld32_x16(tO + uint32_t(c0), o);
-                if (!row_valid) continue;
-#pragma unroll
-                for (int q = 0; q < 16; q += 8) {
-                    if (c0 + q + 8 > p.D || !VF_IN(row0 + c0 + q, 8, p.out_elems, err)) continue;
-                    uint4 v;
-                    v.x = cvt_bf16x2(__uint_as_float(o[q]) * os, __uint_as_float(o[q + 1]) * os);
-                    v.y = cvt_bf16x2(__uint_as_float(o[q + 2]) * os, __uint_as_float(o[q + 3]) * os);
-                    v.z = cvt_bf16x2(__uint_as_float(o[q + 4]) * os, __uint_as_float(o[q + 5]) * os);
-                    v.w = cvt_bf16x2(__uint_as_float(o[q + 6]) * os, __uint_as_float(o[q + 7]) * os);
-                    *reinterpret_cast<uint4*>(orow + c0 + q) = v;
+            store_row2(tO, p, scale_v, (int64_t(qrow) * p.H + h) * p.D, row_valid, err);
+        }
+    }
+
+    // ---- teardown: all TMEM traffic of this CTA is complete past this barrier.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// A unit of the persistent kernel: one 256-query item of the work list.
+struct Unit2 {
+    int h, q0, seg_s, seg_e, kb0, nkv;
+};
+
+// Unit (work item) u -> its rows and key tiles (the calling warp finds the
+// record: every lane must call).
+__device__ __forceinline__ bool decode_unit2(const AttnParams& p, int u, int4 mine, Unit2& w) {
+    SegRec rec;
+    if (!find_item_pick(p, u, mine, rec)) return false;
+    const int local = u - rec.first_item;
+    w.h = local / rec.nq;
+    w.q0 = rec.seg_s + (local - w.h * rec.nq) * (2 * BM);
+    w.seg_s = rec.seg_s;
+    w.seg_e = rec.seg_e;
+    w.kb0 = rec.seg_s & ~15;
+    w.nkv = (rec.seg_e - w.kb0 + BN - 1) / BN;
+    return true;
+}
+
+// The same units run by one CTA per SM: the TMA warp takes units from the
+// call's counter (the first one is blockIdx.x), publishes each in one of two
+// description slots and loads its Q tiles once every S product of the previous
+// unit is done with Q, and its K/V tiles through the ring while the previous
+// unit finishes, so a unit's set-up and first loads overlap the previous
+// unit's last tiles.  Ring stages and the per-tile barrier phases count key
+// tiles across units; a unit's first P.V (which overwrites O) waits for the
+// tile's softmax warps to have read the previous unit's O.  Every unit
+// computes what attn_fp8_2tile_kernel computes for it (same bits).
+template <bool OWN_S>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+attn_fp8_2tile_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                                 const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
+    int32_t* err = &p.ws->error;
+    auto BAR = [&](int i) -> uint32_t { return sb + SM_BAR + 8u * uint32_t(i); };
+    auto INFO = [&](int slot) -> volatile int* {
+        return reinterpret_cast<volatile int*>(smem + SM_INFO + slot * INFO_INTS * 4);
+    };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t vbytes = uint32_t(p.DV) * 128u;
+    auto publish = [&](int slot, const Unit2& w) {
+        volatile int* inf = INFO(slot);
+        inf[I_WORK] = 1;
+        inf[I_H] = w.h;
+        inf[I_Q0] = w.q0;
+        inf[I_SEGS] = w.seg_s;
+        inf[I_SEGE] = w.seg_e;
+        inf[I_KB0] = w.kb0;
+        inf[I_NKV] = w.nkv;
+    };
+
+    // The TMA warp decodes the CTA's first unit; its lane 0 initialises the
+    // barriers, publishes the unit and starts Q_A, Q_B and K tile 0 before
+    // the set-up sync.
+    int4 mine = make_int4(0, 0, 0, 0);
+    int units = 0;
+    Unit2 w0;
+    bool have0 = false;
+    if (warp == WARP_TMA) {
+        mine = find_item_load(p);
+        units = p.ws->total_items;
+        have0 = int(blockIdx.x) < units && decode_unit2(p, blockIdx.x, mine, w0);
+        if (lane == 0) {
+            mbar_init(BAR(B_QFULL), 1);
+            for (int s = 0; s < NST; ++s) {
+                mbar_init(BAR(B_KFULL + s), 1);
+                mbar_init(BAR(B_VFULL + s), 1);
+                mbar_init(BAR(B_KEMPTY + s), 1);
+                mbar_init(BAR(B_VEMPTY + s), 1);
+            }
+            for (int g = 0; g < 2; ++g) {
+                mbar_init(BAR(B_SFULL + g), 1);
+                mbar_init(BAR(B_SFREE + g), 4);
+                mbar_init(BAR(B_PFULL + g), 4);
+                mbar_init(BAR(B_OFULL + g), 1);
+                mbar_init(BAR(B_OFREE + g), 4);
+                mbar_init(BAR(B_IFULL + g), 1);
+                mbar_init(BAR(B_IEMPTY + g), IEMPTY_COUNT);
+            }
+            mbar_init(BAR(B_FINAL), 2);   // one commit per issuer
+            mbar_init(BAR(B_QEMPTY), 1);
+            *abort_flag = 0;
+            fence_mbar_init();
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            if (have0) publish(0, w0);
+            else INFO(0)[I_WORK] = 0;
+            mbar_arrive(BAR(B_IFULL + 0));
+            if (have0 && VF_CHECKED_BUILD && (w0.kb0 & 15) != 0) {
+                record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
+                *abort_flag = 1;
+            } else if (have0) {
+                mbar_arrive_expect_tx(BAR(B_QFULL), 2 * QBYTES);
+                tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, w0.h, w0.q0);
+                tma_load_3d(sb + SM_Q + QBYTES, &tmQ, BAR(B_QFULL), 0, w0.h, w0.q0 + BM);
+                mbar_arrive_expect_tx(BAR(B_KFULL + 0), KBYTES);
+                tma_load_3d(sb + SM_K, &tmK, BAR(B_KFULL + 0), 0, w0.h, w0.kb0);
+            }
+        }
+    }
+
+    uint32_t tmem = 0;
+    if (warp == WARP_TMA) {
+        __syncwarp();
+        __threadfence_block();
+        named_bar_arrive<1, NUM_THREADS>();
+    } else {
+        const int t = threadIdx.x < 32 * WARP_TMA ? threadIdx.x : threadIdx.x - 32;
+        for (int i = t; i < NST * 16 * 32; i += NUM_THREADS - 32) {
+            const int blk = i / (16 * 32);
+            const int wd = i - blk * (16 * 32);
+            if (VF_IN(blk * VBLK + p.DV * 128 + 4 * wd, 4, NST * VBLK, err))
+                reinterpret_cast<uint32_t*>(smem + SM_V + blk * VBLK + p.DV * 128)[wd] = 0x38383838u;
+        }
+        fence_proxy_async_smem();
+        if (warp == WARP_MMA) {
+            tmem_alloc(sb + SM_TMEMPTR, TMEM_COLS);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        named_bar_sync<1, NUM_THREADS>();
+        tc_fence_after();
+        tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEMPTR);
+    }
+
+    if (warp >= 8) {
+        regs_decrease<REGS_PRODUCER>();
+        if (warp == WARP_TMA) {
+            // ------------------------------------------------ TMA producer
+            int gt = 0;            // key tiles whose K/V copies were started (across units)
+            int kq = 0;            // units whose Q copies were started
+            bool k_only = false;   // K of tile gt started, its V not
+            bool ok = !*abort_flag;
+            Unit2 w = w0;
+            bool have = have0;
+            for (int qi = 0; ok && have; ++qi) {
+                if (lane == 0) {
+                    const int slot = qi & 1;
+                    if (qi > 0) {
+                        if (qi >= 2) ok = bwait(BAR(B_IEMPTY + slot), ((qi - 2) >> 1) & 1, abort_flag, err);
+                        if (ok) {
+                            publish(slot, w);
+                            mbar_arrive(BAR(B_IFULL + slot));
+                            if (VF_CHECKED_BUILD && (w.kb0 & 15) != 0) {
+                                record_error(err, VITFP8_ERR_DEVICE_BOUNDS);
+                                *abort_flag = 1;
+                                ok = false;
+                            } else if ((ok = bwait(BAR(B_QEMPTY), (qi - 1) & 1, abort_flag, err))) {
+                                mbar_arrive_expect_tx(BAR(B_QFULL), 2 * QBYTES);
+                                tma_load_3d(sb + SM_Q, &tmQ, BAR(B_QFULL), 0, w.h, w.q0);
+                                tma_load_3d(sb + SM_Q + QBYTES, &tmQ, BAR(B_QFULL), 0, w.h, w.q0 + BM);
+                            }
+                        }
+                    }
+                    if (ok) ++kq;
+                    for (int j = 0; ok && j < w.nkv; ++j, ++gt) {
+                        const int s = gt % NST;
+                        const int key0 = w.kb0 + j * BN;
+                        if (!(qi == 0 && j == 0)) {   // K tile 0 of the first unit went out at set-up
+                            if (gt >= NST && !(ok = bwait(BAR(B_KEMPTY + s), ((gt / NST) - 1) & 1, abort_flag, err)))
+                                break;
+                            mbar_arrive_expect_tx(BAR(B_KFULL + s), KBYTES);
+                            tma_load_3d(sb + SM_K + s * KBYTES, &tmK, BAR(B_KFULL + s), 0, w.h, key0);
+                        }
+                        if (gt >= NST && !(ok = bwait(BAR(B_VEMPTY + s), ((gt / NST) - 1) & 1, abort_flag, err))) {
+                            k_only = true;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(BAR(B_VFULL + s), vbytes);
+                        tma_load_3d(sb + SM_V + s * VBLK, &tmV, BAR(B_VFULL + s), key0, 0, w.h);
+                    }
                 }
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                // The next unit: every lane takes part in the record vote.
+                int nu = 0;
+                if (lane == 0) nu = int(gridDim.x) + atomicAdd(&p.ws->next_unit, 1);
+                nu = __shfl_sync(0xFFFFFFFFu, nu, 0);
+                have = nu < units && decode_unit2(p, nu, mine, w);
+                if (!have && lane == 0) {
+                    // "No more work" in the next slot, once it is free.
+                    const int slot = (qi + 1) & 1;
+                    if (qi + 1 < 2 || bwait(BAR(B_IEMPTY + slot), ((qi - 1) >> 1) & 1, abort_flag, err)) {
+                        INFO(slot)[I_WORK] = 0;
+                        mbar_arrive(BAR(B_IFULL + slot));
+                    }
+                }
+            }
+            if (lane == 0 && *abort_flag) {
+                // Let the copies this thread started land before the CTA
+                // exits (bounded spins; these barriers were armed).
+                for (int spin = 0; spin < (1 << 22) && kq > 0; ++spin)
+                    if (mbar_try_wait(BAR(B_QFULL), (kq - 1) & 1)) break;
+                const int gk = gt + (k_only ? 1 : 0);
+                for (int gg = (gk > NST ? gk - NST : 0); gg < gk; ++gg) {
+                    const int s = gg % NST;
+                    const uint32_t ph = (gg / NST) & 1;
+                    for (int spin = 0; spin < (1 << 22); ++spin)
+                        if (mbar_try_wait(BAR(B_KFULL + s), ph)) break;
+                    for (int spin = 0; spin < (1 << 22) && gg < gt; ++spin)
+                        if (mbar_try_wait(BAR(B_VFULL + s), ph)) break;
+                }
+            }
+        } else if (warp == WARP_MMA) {
+            // ------------------------------------------------ S issuer
+            if (lane == 0) {
+                const uint32_t idS = make_idesc(0, BM, BN);
+                const uint64_t dQA = sw128_kmajor_desc(sb + SM_Q);
+                const uint64_t dQB = sw128_kmajor_desc(sb + SM_Q + QBYTES);
+                const uint64_t dK0 = sw128_kmajor_desc(sb + SM_K);
+                const int KS = p.KS;
+                auto issue_S = [&](uint64_t dQ, int s, int g) {
+                    const uint32_t tS = tmem + tm_s<OWN_S>(g);
+                    const uint64_t dk = dK0 + uint64_t(s * (KBYTES >> 4));
+                    if (KS == 4) {
+                        umma_f8_ss_k4(tS, dQ, dk, idS, 0u);
+                    } else {
+                        umma_f8(tS, dQ, dk, idS, 0u);
+                        for (int kk = 1; kk < KS; ++kk)
+                            umma_f8(tS, dQ + uint64_t(2 * kk), dk + uint64_t(2 * kk), idS, 1u);
+                    }
+                };
+                // Key tile gt (counted across units) uses ring stage gt % NST
+                // in phase (gt / NST) & 1; its S / P / O barriers, parity gt & 1.
+                int gt = 0;
+                bool ok = true;
+                for (int qi = 0; ok; ++qi) {
+                    const int slot = qi & 1;
+                    if (!(ok = bwait(BAR(B_IFULL + slot), (qi >> 1) & 1, abort_flag, err))) break;
+                    if (!INFO(slot)[I_WORK]) break;
+                    const int nkv = INFO(slot)[I_NKV];
+                    if (!(ok = bwait(BAR(B_QFULL), qi & 1, abort_flag, err))) break;
+                    for (int j = 0; j < nkv; ++j, ++gt) {
+                        const int s = gt % NST;
+                        const uint32_t par = uint32_t(gt) & 1u;
+                        if (!(ok = bwait(BAR(B_KFULL + s), (gt / NST) & 1, abort_flag, err))) break;
+                        if (OWN_S) {
+                            if (gt > 0 && !(ok = bwait(BAR(B_SFREE + 0), par ^ 1u, abort_flag, err))) break;
+                            tc_fence_after();
+                            issue_S(dQA, s, 0);
+                            tc_commit(BAR(B_SFULL + 0));
+                            if (gt > 0 && !(ok = bwait(BAR(B_SFREE + 1), par ^ 1u, abort_flag, err))) break;
+                            tc_fence_after();
+                            issue_S(dQB, s, 1);
+                        } else {
+                            if (gt > 0 && !(ok = bwait(BAR(B_SFREE + 1), par ^ 1u, abort_flag, err))) break;
+                            tc_fence_after();
+                            issue_S(dQA, s, 0);
+                            tc_commit(BAR(B_SFULL + 0));
+                            if (!(ok = bwait(BAR(B_SFREE + 0), par, abort_flag, err))) break;
+                            tc_fence_after();
+                            issue_S(dQB, s, 1);
+                        }
+                        tc_commit(BAR(B_SFULL + 1));
+                        tc_commit(BAR(B_KEMPTY + s));
+                    }
+                    if (!ok) break;
+                    tc_commit(BAR(B_QEMPTY));   // every S product of this unit read Q
+                    mbar_arrive(BAR(B_IEMPTY + slot));
+                }
+                tc_commit(BAR(B_FINAL));
+                for (int spin = 0; spin < (1 << 24); ++spin)
+                    if (mbar_try_wait(BAR(B_FINAL), 0)) break;
+            }
+        } else if (warp == WARP_PV) {
+            // ------------------------------------------------ P.V issuer
+            if (lane == 0) {
+                const uint32_t idPV = make_idesc(0, BM, p.DV + 16);
+                const uint64_t dV0 = sw128_kmajor_desc(sb + SM_V);
+                int gt = 0;
+                bool ok = true;
+                for (int qi = 0; ok; ++qi) {
+                    const int slot = qi & 1;
+                    if (!(ok = bwait(BAR(B_IFULL + slot), (qi >> 1) & 1, abort_flag, err))) break;
+                    if (!INFO(slot)[I_WORK]) break;
+                    const int nkv = INFO(slot)[I_NKV];
+                    for (int j = 0; ok && j < nkv; ++j, ++gt) {
+                        const int s = gt % NST;
+                        if (!(ok = bwait(BAR(B_VFULL + s), (gt / NST) & 1, abort_flag, err))) break;
+                        const uint64_t dv = dV0 + uint64_t(s * (VBLK >> 4));
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            if (!(ok = bwait(BAR(B_PFULL + g), uint32_t(gt) & 1u, abort_flag, err))) break;
+                            // A unit's first product overwrites O: once the tile's
+                            // softmax has read the previous unit's O.
+                            if (j == 0 && qi > 0 && !(ok = bwait(BAR(B_OFREE + g), (qi - 1) & 1, abort_flag, err)))
+                                break;
+                            tc_fence_after();
+                            umma_f8_ts_k4(tmem + tm_o<OWN_S>(g), tmem + tm_p<OWN_S>(g), dv, idPV, j > 0 ? 1u : 0u);
+                            tc_commit(BAR(B_OFULL + g));
+                        }
+                        if (!ok) break;
+                        tc_commit(BAR(B_VEMPTY + s));
+                    }
+                    if (!ok) break;
+                    mbar_arrive(BAR(B_IEMPTY + slot));
+                }
+                tc_commit(BAR(B_FINAL));
+                for (int spin = 0; spin < (1 << 24); ++spin)
+                    if (mbar_try_wait(BAR(B_FINAL), 0)) break;
+            }
+        }
+    } else {
+        // ------------------------------------------------ softmax (warps 0..7)
+        regs_increase<REGS_SOFTMAX>();
+        const int g = warp >> 2;
+        const int rbase = 32 * (warp & 3);
+        const uint32_t lane_off = uint32_t(rbase) << 16;
+        const uint32_t tS = tmem + lane_off + tm_s<OWN_S>(g);
+        const uint32_t tO = tmem + lane_off + tm_o<OWN_S>(g);
+        const uint32_t tP = tmem + lane_off + tm_p<OWN_S>(g);
+        const float c = p.st->scale[0] * p.st->scale[1] * p.sm_scale * 1.4426950408889634f;
+        const uint64_t c2 = f32x2_pack(c, c);
+        const float scale_v = p.st->scale[2];
+        const Tile2 tx{tS, tO, tP, sb + SM_BAR, c2, c, p.DV + 16, g, abort_flag, err};
+        int gt = 0;
+        bool ok = true;
+        for (int qi = 0; ok; ++qi) {
+            const int slot = qi & 1;
+            ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_IFULL + slot), (qi >> 1) & 1, abort_flag, err));
+            if (!ok) break;
+            // The unit's description, broadcast from lane 0 (warp-uniform values).
+            if (!__shfl_sync(0xFFFFFFFFu, INFO(slot)[I_WORK], 0)) break;
+            const int h = __shfl_sync(0xFFFFFFFFu, INFO(slot)[I_H], 0);
+            const int q0 = __shfl_sync(0xFFFFFFFFu, INFO(slot)[I_Q0], 0);
+            const int seg_s = __shfl_sync(0xFFFFFFFFu, INFO(slot)[I_SEGS], 0);
+            const int seg_e = __shfl_sync(0xFFFFFFFFu, INFO(slot)[I_SEGE], 0);
+            const int kb0 = __shfl_sync(0xFFFFFFFFu, INFO(slot)[I_KB0], 0);
+            const int nkv = __shfl_sync(0xFFFFFFFFu, INFO(slot)[I_NKV], 0);
+            float m_ref = 0.0f;
+            for (int j = 0; j < nkv; ++j, ++gt) {
+                ok = softmax_tile2(tx, kb0 + j * BN, seg_s, seg_e, j == 0, uint32_t(gt) & 1u, m_ref);
+                if (!ok) break;
+            }
+            if (ok) ok = __all_sync(0xFFFFFFFFu, bwait(BAR(B_OFULL + g), uint32_t(gt - 1) & 1u, abort_flag, err));
+            if (!ok) break;
+            tc_fence_after();
+            const int qrow = q0 + g * BM + rbase + lane;
+            store_row2(tO, p, scale_v, (int64_t(qrow) * p.H + h) * p.D, qrow < seg_e, err);
+            // O has been read: the next unit's first P.V may overwrite it.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(BAR(B_OFREE + g));
+                mbar_arrive(BAR(B_IEMPTY + slot));
             }
         }
     }
@@ -501,7 +910,7 @@ PerDeviceOnce g_smem_attr;
 }  // namespace tt
 
 vitfp8_status launch_attn_fp8_2tile(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                    const AttnParams& prm, int nsm, cudaStream_t s) {
+                                    const AttnParams& prm, int nsm, bool persistent, cudaStream_t s) {
     using namespace tt;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return VITFP8_ERR_CUDA;
@@ -511,16 +920,29 @@ vitfp8_status launch_attn_fp8_2tile(const CUtensorMap& mq, const CUtensorMap& mk
             return cudaFuncSetAttribute(attn_fp8_2tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         SMEM_BYTES) == cudaSuccess &&
                    cudaFuncSetAttribute(attn_fp8_2tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES) == cudaSuccess;
+                                        SMEM_BYTES) == cudaSuccess &&
+                   cudaFuncSetAttribute(attn_fp8_2tile_persistent_kernel<false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess &&
+                   cudaFuncSetAttribute(attn_fp8_2tile_persistent_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess;
         }))
         return VITFP8_ERR_CUDA;
     // Work units are at most (T / 256 + nseq) * H; CTAs without one return at once.
     const long long units = (long long)((prm.T + 2 * BM - 1) / (2 * BM) + prm.nseq) * prm.H;
     if (units > 0x7FFFFFFFLL) return VITFP8_ERR_UNSUPPORTED;
-    if (prm.DV + 16 <= OWN_S_MAX_OCOLS)
+    const bool own_s = prm.DV + 16 <= OWN_S_MAX_OCOLS;
+    if (persistent) {
+        // One CTA per SM taking units from the counter the plan zeroed.
+        const unsigned grid = unsigned(units < nsm ? units : nsm);
+        if (own_s)
+            attn_fp8_2tile_persistent_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);
+        else
+            attn_fp8_2tile_persistent_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);
+    } else if (own_s) {
         attn_fp8_2tile_kernel<true><<<unsigned(units), NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);
-    else
+    } else {
         attn_fp8_2tile_kernel<false><<<unsigned(units), NUM_THREADS, SMEM_BYTES, s>>>(mq, mk, mv, prm);
+    }
     return cudaGetLastError() == cudaSuccess ? VITFP8_OK : VITFP8_ERR_CUDA;
 }
 

@@ -89,28 +89,30 @@ constexpr int kAttnAuto = 0;        // attn_fp8_kernel_for() picks
 constexpr int kAttnUnit = 1;        // one CTA per 128-row work item (attn_fp8.cu)
 constexpr int kAttnPersistent = 2;  // one CTA per SM walking the work items (attn_fp8.cu)
 constexpr int kAttnTwoTile = 3;     // one CTA per 256-row unit, two query tiles (attn_fp8_2tile.cu)
-// Two-tile kernel: longest segment at least this long, at least kTwoTileMinWaves
-// waves of 256-row units, and the last wave's shortfall at most
+constexpr int kAttnTwoTilePersistent = 4;  // the two-tile units run by one CTA per SM
+// Two-tile kernels: at least kTwoTileMinWaves waves of 256-row units; for
+// segments of kTwoTileLongSeqlen tokens or more (where the two-tile kernels
+// gain only a few per cent per unit) also the last wave's shortfall at most
 // kTwoTileMaxTail of the time (ceil(w) / w <= 1 + kTwoTileMaxTail).
-constexpr int kTwoTileMinSeqlen = 2048;
+constexpr int kTwoTileLongSeqlen = 2048;
 constexpr double kTwoTileMinWaves = 2.0;
 constexpr double kTwoTileMaxTail = 0.12;
-// Persistent kernel: longest segment at most this long and more than one wave of items.
+// Persistent kernels: longest segment at most this long (the one-tile one also
+// needs more than one wave of items).
 constexpr int kPersistentMaxSeqlen = 6144;
 
 // The kernel the FP8 attention call runs when none is asked for, from what
 // the host knows: segment count, the bound on segment lengths, token count,
-// heads and SM count.  The two-tile kernel's units are estimated as
+// heads and SM count.  The two-tile kernels' units are estimated as
 // H * (T + 128 * nseq) / 256 (a segment's last unit is half full on average).
 inline int attn_fp8_kernel_for(int nseq, int max_seqlen, int T, int H, int nsm) {
     if (nsm <= 0 || nseq <= 0 || T <= 0 || H <= 0) return kAttnUnit;
-    if (max_seqlen >= kTwoTileMinSeqlen) {
-        const double waves = double(H) * (double(T) + 128.0 * nseq) / 256.0 / double(nsm);
-        if (waves >= kTwoTileMinWaves) {
-            double full = double(int64_t(waves));
-            if (full < waves) full += 1.0;
-            if (full <= waves * (1.0 + kTwoTileMaxTail)) return kAttnTwoTile;
-        }
+    const double waves = double(H) * (double(T) + 128.0 * nseq) / 256.0 / double(nsm);
+    if (waves >= kTwoTileMinWaves) {
+        double full = double(int64_t(waves));
+        if (full < waves) full += 1.0;
+        if (max_seqlen < kTwoTileLongSeqlen || full <= waves * (1.0 + kTwoTileMaxTail))
+            return max_seqlen <= kPersistentMaxSeqlen ? kAttnTwoTilePersistent : kAttnTwoTile;
     }
     const long long max_items = (long long)((T + 127) / 128 + nseq) * H;
     if (max_seqlen <= kPersistentMaxSeqlen && max_items > nsm) return kAttnPersistent;

@@ -253,7 +253,7 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs);
  *          word and the partial results of a key-range split.  Calls sharing
  *          one workspace must be stream-ordered.
  *
- * Scheduling (vitfp8_attn_kernel_for picks one of three kernels; all compute
+ * Scheduling (vitfp8_attn_kernel_for picks one of four kernels; all compute
  * the attention above):
  *  - VITFP8_ATTN_UNIT: one CTA per 128-query tile of a (segment, head).  When
  *    the tiles leave a last wave that fills at most half the GPU, the key range
@@ -266,6 +266,9 @@ size_t vitfp8_attn_workspace_size(int32_t num_seqs);
  *    sharing each key tile), for long segments whose units fill the GPU's
  *    waves well.  Its reference moves at 128-key boundaries, so about 1 % of
  *    the outputs can differ from the other kernels' in the last bf16 bit.
+ *  - VITFP8_ATTN_TWO_TILE_PERSISTENT: the same units run by one CTA per SM
+ *    (for segments of up to 6144 tokens); the same bits as
+ *    VITFP8_ATTN_TWO_TILE.
  * The result is deterministic for a given input, max_seqlen and GPU.
  */
 vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
@@ -280,6 +283,7 @@ vitfp8_status vitfp8_attn_varlen(const uint8_t* q8, const uint8_t* k8, const uin
 #define VITFP8_ATTN_UNIT 1       /* one CTA per 128-query work item */
 #define VITFP8_ATTN_PERSISTENT 2 /* one CTA per SM walking the work items */
 #define VITFP8_ATTN_TWO_TILE 3   /* one CTA per 256-query unit */
+#define VITFP8_ATTN_TWO_TILE_PERSISTENT 4 /* the 256-query units run by one CTA per SM */
 
 /*
  * vitfp8_attn_varlen with the kernel named by `kernel` (one of the
@@ -297,10 +301,12 @@ vitfp8_status vitfp8_attn_varlen_kernel(const uint8_t* q8, const uint8_t* k8, co
 
 /*
  * The kernel vitfp8_attn_varlen runs for these sizes on a GPU with num_sms
- * SMs (host only, no device call):
- *  - VITFP8_ATTN_TWO_TILE when max_seqlen >= 2048 and the estimated 256-query
- *    units, w = H (T + 128 num_seqs) / 256 / num_sms waves, are at least two
- *    waves with ceil(w) / w <= 1.12 (the last wave nearly full);
+ * SMs (host only, no device call).  With w = H (T + 128 num_seqs) / 256 /
+ * num_sms, the estimated waves of 256-query units:
+ *  - a two-tile kernel when w >= 2 and either max_seqlen < 2048 or
+ *    ceil(w) / w <= 1.12 (the last wave nearly full): the persistent one
+ *    (VITFP8_ATTN_TWO_TILE_PERSISTENT) when max_seqlen <= 6144, else
+ *    VITFP8_ATTN_TWO_TILE;
  *  - else VITFP8_ATTN_PERSISTENT when max_seqlen <= 6144 and the 128-query
  *    items, (ceil(T / 128) + num_seqs) H, are more than num_sms;
  *  - else VITFP8_ATTN_UNIT (also for non-positive sizes).

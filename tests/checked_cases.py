@@ -95,6 +95,8 @@ def run_cases(vf):
         ("tt128", [300, 1000, 129, 1], 2, 128, 48, True, "packed", "two_tile"),
         ("tt80", [600, 77, 256], 3, 80, 49, True, "padded", "two_tile"),
         ("tt40", [3, 130, 61, 700], 2, 40, 50, True, "packed", "two_tile"),
+        ("ttp", [700, 1, 256, 300, 1500], 4, 128, 51, True, "packed", "two_tile_persistent"),
+        ("ttp80", [511, 0, 257], 6, 80, 52, True, "packed", "two_tile_persistent"),
     ]
     for D in range(8, 129, 8):
         cases.append(("d%d" % D, [3, 130, 61], 2, D, 100 + D, D % 16 == 0, "packed"))

@@ -1,16 +1,17 @@
-"""The FP8 attention call runs one of three kernels (the library's choice, or
+"""The FP8 attention call runs one of four kernels (the library's choice, or
 the one named by ``kernel=``):
 
 * "unit": one CTA per 128-query work item;
 * "persistent": one CTA per SM walking the same work items;
 * "two_tile": one CTA per 256-query unit, two query tiles sharing each key
-  tile (one S buffer for d > 80, one per tile for d <= 80).
+  tile (one S buffer for d > 80, one per tile for d <= 80);
+* "two_tile_persistent": one CTA per SM walking the same 256-query units.
 
 The unit and persistent kernels do the same arithmetic for every item, so
-their outputs are bit-identical.  The two-tile kernel moves a row's reference
-at 128-key boundaries; its outputs are checked against the fp64 oracle under
-the same bound as every other case, and against the unit kernel (almost all
-outputs identical).  The BF16 path has the unit and persistent kernels,
+their outputs are bit-identical, and so are the two two-tile kernels.  The
+two-tile kernels move a row's reference at 128-key boundaries; their outputs
+are checked against the fp64 oracle under the same bound as every other
+case, and against the unit kernel (almost all outputs identical).  The BF16 path has the unit and persistent kernels,
 chosen by max_seqlen (an upper bound on the segment lengths, so a larger one
 runs the other kernel on the same inputs).
 """
@@ -97,6 +98,8 @@ def test_kernels_agree(vf, name, seqlens, H, D):
     pers = _run(vf, c, seqlens, D, "persistent")
     assert torch.equal(unit.view(torch.int16), pers.view(torch.int16))
     two = _run(vf, c, seqlens, D, "two_tile")
+    two_p = _run(vf, c, seqlens, D, "two_tile_persistent")
+    assert torch.equal(two.view(torch.int16), two_p.view(torch.int16))
     _oracle_check(c, pers, seqlens, D, name)
     _oracle_check(c, two, seqlens, D, name + " two-tile")
     _close_to(two, unit)
@@ -104,7 +107,8 @@ def test_kernels_agree(vf, name, seqlens, H, D):
 
 def test_auto_runs_the_rule(vf):
     """attn_varlen without a kernel gives the bits of the kernel the stated rule names."""
-    for seqlens, H, D in (([3600] * 3, 16, 80), ([300, 200], 2, 128), ([1024] * 8, 16, 64)):
+    for seqlens, H, D in (([3600] * 3, 16, 80), ([300, 200], 2, 128), ([1024] * 8, 16, 64),
+                          ([1024] * 8, 5, 64), ([8192], 16, 128)):
         c = _codes(vf, seqlens, H, D, 7)
         name = vf.attn_kernel_for(len(seqlens), max(seqlens), sum(seqlens), H, nsm())
         auto = _run(vf, c, seqlens, D, "auto")
@@ -161,6 +165,8 @@ def test_random_batches_agree(vf, case):
     pers = _run(vf, c, seqlens, D, "persistent")
     assert torch.equal(unit.view(torch.int16), pers.view(torch.int16)), case
     two = _run(vf, c, seqlens, D, "two_tile")
+    two_p = _run(vf, c, seqlens, D, "two_tile_persistent")
+    assert torch.equal(two.view(torch.int16), two_p.view(torch.int16)), case
     T = sum(seqlens)
     rows = np.random.default_rng(case).choice(T, min(T, 300), replace=False)
     for out, tag in ((unit, "unit"), (two, "two-tile")):

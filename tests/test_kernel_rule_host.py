@@ -24,7 +24,7 @@ def _const(name):
     return float(m.group(1))
 
 
-MIN_SEQLEN = _const("kTwoTileMinSeqlen")
+LONG_SEQLEN = _const("kTwoTileLongSeqlen")
 MIN_WAVES = _const("kTwoTileMinWaves")
 MAX_TAIL = _const("kTwoTileMaxTail")
 PERSISTENT_MAX = _const("kPersistentMaxSeqlen")
@@ -33,10 +33,9 @@ PERSISTENT_MAX = _const("kPersistentMaxSeqlen")
 def expected_kernel(nseq, max_seqlen, T, H, nsm):
     if nsm <= 0 or nseq <= 0 or T <= 0 or H <= 0:
         return "unit"
-    if max_seqlen >= MIN_SEQLEN:
-        w = H * (T + 128.0 * nseq) / 256.0 / nsm
-        if w >= MIN_WAVES and math.ceil(w) <= w * (1.0 + MAX_TAIL):
-            return "two_tile"
+    w = H * (T + 128.0 * nseq) / 256.0 / nsm
+    if w >= MIN_WAVES and (max_seqlen < LONG_SEQLEN or math.ceil(w) <= w * (1.0 + MAX_TAIL)):
+        return "two_tile_persistent" if max_seqlen <= PERSISTENT_MAX else "two_tile"
     items = (-(-T // 128) + nseq) * H
     if max_seqlen <= PERSISTENT_MAX and items > nsm:
         return "persistent"
@@ -50,19 +49,22 @@ def vf():
 
 
 def test_constants():
-    assert (MIN_SEQLEN, MIN_WAVES, MAX_TAIL, PERSISTENT_MAX) == (2048, 2.0, 0.12, 6144)
+    assert (LONG_SEQLEN, MIN_WAVES, MAX_TAIL, PERSISTENT_MAX) == (2048, 2.0, 0.12, 6144)
 
 
 def test_pages_workloads_on_152_sms(vf):
     import workloads
-    want = {"tiny": "unit", "micro8k": "unit", "hd3": "two_tile", "qhd3": "two_tile",
+    want = {"tiny": "unit", "micro8k": "unit", "hd3": "two_tile_persistent", "qhd3": "two_tile",
             "uhd3mix": "two_tile"}
     for name, k in want.items():
         w = workloads.WORKLOADS[name]
         assert vf.attn_kernel_for(len(w.seqlens), w.max_seqlen, w.T, w.H, 152) == k, name
-    # many short segments: the persistent kernel
-    assert vf.attn_kernel_for(8, 1024, 8192, 16, 152) == "persistent"
-    assert vf.attn_kernel_for(200, 256, 51200, 4, 152) == "persistent"
+    # many short segments: the persistent two-tile kernel
+    assert vf.attn_kernel_for(8, 1024, 8192, 16, 152) == "two_tile_persistent"
+    assert vf.attn_kernel_for(200, 256, 51200, 4, 152) == "two_tile_persistent"
+    # short segments but under two waves of 256-query units: the one-tile kernels
+    assert vf.attn_kernel_for(8, 1024, 8192, 2, 152) == "unit"
+    assert vf.attn_kernel_for(8, 1024, 8192, 5, 152) == "persistent"
     # a last wave a third full: one CTA per item (8192 tokens, 16 heads: 3.4 waves of units)
     assert vf.attn_kernel_for(1, 8192, 8192, 16, 152) == "unit"
     # degenerate sizes
