@@ -375,7 +375,8 @@ def attn_varlen(q8, k8, v8t, state, cu_seqlens, max_seqlen, D, sm_scale=None, ou
                 workspace=None, stream=None, kernel="auto"):
     """FP8 varlen attention -> bf16 [T, H, D].
 
-    kernel: "auto" (the library's choice), "unit", "persistent" or "two_tile"."""
+    kernel: "auto" (the library's choice), "unit", "persistent", "two_tile" or
+    "two_tile_persistent" (vitfp8_attn_varlen_kernel)."""
     nseq = _cu_info(cu_seqlens)
     T, H, D_pad = _check_codes(q8, k8, v8t)
     if sm_scale is None:
