@@ -54,6 +54,12 @@ ATTN_FP8_SOURCES = ["attn_fp8.cu", "attn_fp8_2tile.cu", "attn_common.cuh", "chec
 QUANT_SOURCES = ["quant.cu", "checked.cuh", "internal.cuh", "ptx.cuh"]
 
 
+def _fp8_kernel(vf, seqlens, H, dev):
+    """Name of the FP8 attention kernel the library picks for these segments."""
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    return vf.attn_kernel_for(len(seqlens), max(seqlens), sum(seqlens), H, nsm)
+
+
 def _profile_traffic(md_name, sources):
     """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged."""
     import hashlib
@@ -372,6 +378,7 @@ def resolution_sweep(vf, dev, stream, reps, head_dims=(80, 128), H=16, images=3,
             flops = 4 * images * L * L * H * D
             row = {
                 "sweep": name, "tokens_per_image": L, "images": images, "heads": H, "head_dim": D,
+                "fp8_kernel": _fp8_kernel(vf, [L] * images, H, dev),
                 **{k2 + "_us": round(v2, 1) for k2, v2 in res.items()},
                 "fp8_dynamic_vs_bf16": round(res["bf16"] / res["fp8_dynamic"], 3),
                 "fp8_static_vs_bf16": round(res["bf16"] / res["fp8_static"], 3),
@@ -444,6 +451,7 @@ def per_config_block(vf, dev, stream, peaks, peak_kind, reps=None):
         block[name] = {
             "workload": w.desc, "scaling": "dynamic" if run.dynamic else "static",
             "tokens": w.T, "heads": w.H, "head_dim": w.D, "flops": flops,
+            "fp8_kernel": _fp8_kernel(vf, w.seqlens, w.H, dev),
             "fp8_attn_us": round(res["fp8_attn"], 1), "fp8_attn_tflops": round(fp8_tf, 1),
             "fp8_attn_frac_of_peak": round(fp8_tf / fp8_peak, 4),
             "quant_us": round(res["quant"], 1), "quant_bytes": qbytes,
@@ -590,7 +598,8 @@ def main():
                           ("L2 flushed (a %d MB write, read back) before every timed step, outside the timed "
                            "spans; a step reads %.0f MB of bf16 q/k/v" % (L2_FLUSH_BYTES >> 20,
                                                                           step_bytes / 1e6))),
-                   "parallelism": "replicas" if ws > 1 else "single"},
+                   "parallelism": "replicas" if ws > 1 else "single",
+                   "fp8_kernel": _fp8_kernel(vf, w.seqlens, w.H, dev)},
         "frac_of_fp8_peak": value / fp8_peak,
         "roofline": {"bound": "tensor", "kernel": "attn_fp8 (work-list + attention launch)",
                      "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
