@@ -102,6 +102,23 @@ int main(int argc, char** argv) {
     }
     fclose(in);
 
+    /* The last forward's codes through each named kernel (unit, persistent,
+     * two-tile, persistent two-tile), and the kernel the host rule picks. */
+    vitfp8_bf16* h_kout = (vitfp8_bf16*)malloc(4 * n_elem * sizeof(vitfp8_bf16));
+    vitfp8_bf16* d_kout;
+    if (!h_kout) return 1;
+    CK_CUDA(cudaMalloc((void**)&d_kout, 4 * n_elem * sizeof(vitfp8_bf16)));
+    for (int32_t kern = VITFP8_ATTN_UNIT; kern <= VITFP8_ATTN_TWO_TILE_PERSISTENT; ++kern)
+        CK_VF(vitfp8_attn_varlen_kernel(d_q8, d_k8, d_v8t, d_state, d_cu, nseq, max_seqlen, T, H, D, Dp,
+                                        sm_scale, d_kout + (size_t)(kern - 1) * n_elem, d_ws, ws_bytes,
+                                        kern, s));
+    if (vitfp8_attn_varlen_kernel(d_q8, d_k8, d_v8t, d_state, d_cu, nseq, max_seqlen, T, H, D, Dp, sm_scale,
+                                  d_kout, d_ws, ws_bytes, 99, s) != VITFP8_ERR_INVALID_ARG)
+        return 5;
+    int32_t picked = vitfp8_attn_kernel_for(nseq, max_seqlen, T, H, 152);
+    if (picked < VITFP8_ATTN_UNIT || picked > VITFP8_ATTN_TWO_TILE_PERSISTENT) return 6;
+    CK_CUDA(cudaMemcpyAsync(h_kout, d_kout, 4 * n_elem * sizeof(vitfp8_bf16), cudaMemcpyDeviceToHost, s));
+
     /* Calibrate once from C: the scale-file values of this state (margin 1.5). */
     float* d_saved;
     float h_saved[3];
@@ -119,7 +136,8 @@ int main(int argc, char** argv) {
     if (!out) return 1;
     if (fwrite(&h_state, sizeof(h_state), 1, out) != 1 ||
         fwrite(h_out, sizeof(vitfp8_bf16), n_elem, out) != n_elem ||
-        fwrite(h_saved, sizeof(float), 3, out) != 3)
+        fwrite(h_saved, sizeof(float), 3, out) != 3 ||
+        fwrite(h_kout, sizeof(vitfp8_bf16), 4 * n_elem, out) != 4 * n_elem)
         return 1;
     fclose(out);
     printf("vitfp8 %d: device error %d, workspace error %d\n", vitfp8_version(), dev_err, ws_err);

@@ -1,9 +1,10 @@
 """GPU: the library driven from plain C through its ABI alone.
 
 tests/c_client/vitfp8_client.c allocates with cudaMalloc, runs dynamic
-scaling, quantization and attention for a few forwards, takes the
+scaling, quantization and attention for a few forwards, runs the last
+forward's codes through each named attention kernel, takes the
 calibrate-once scale-file values of the state on the device, and writes the
-scale state, the output and those values; all are compared with the oracle.
+scale state, the outputs and those values; all are compared with the oracle.
 """
 
 import math
@@ -81,3 +82,12 @@ def test_plain_c_client_matches_oracle(tmp_path):
              for t, x in enumerate((q, k, v))]
     stats = compare_attention(out, codes[0], codes[1], codes[2], list(ost.scale), [int(x) for x in cu], D)
     assert_attention_ok(stats, "C client", outliers=True)
+    # the same codes through vitfp8_attn_varlen_kernel with each named kernel:
+    # unit and persistent give the same bits, the two two-tile forms too, and
+    # every one is within the bound of the oracle
+    kout = np.frombuffer(raw[nst + nout + 12:nst + nout + 12 + 4 * nout], dtype=np.int16).reshape(4, T, H, D)
+    assert np.array_equal(kout[0], kout[1]) and np.array_equal(kout[2], kout[3])
+    for i, name in enumerate(("unit", "persistent", "two-tile", "persistent two-tile")):
+        o = torch.from_numpy(kout[i].copy()).view(torch.bfloat16)
+        stats = compare_attention(o, codes[0], codes[1], codes[2], list(ost.scale), [int(x) for x in cu], D)
+        assert_attention_ok(stats, "C client, " + name, outliers=True)
