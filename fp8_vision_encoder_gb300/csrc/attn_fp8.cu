@@ -12,9 +12,11 @@
 // attn_fp8_kernel runs one unit per CTA; attn_fp8_persistent_kernel runs one
 // CTA per SM that takes units from a counter, its TMA warp loading the next
 // unit's Q and K/V tiles while the current unit finishes, so a unit's set-up
-// and first loads overlap the previous unit's last tiles.  The host takes the
-// persistent kernel for segments of up to 6144 tokens, where that fixed cost
-// weighs most, when there is more than one wave of work items.  Roles:
+// and first loads overlap the previous unit's last tiles.  The two-tile
+// kernels (attn_fp8_2tile.cu) run 256-query units with the same arithmetic;
+// attn_fp8_kernel_for (internal.cuh) picks one of the four kernels for a call
+// (this file's for fewer than two waves of 256-query units, or for long
+// segments whose last wave of such units would be far from full).  Roles:
 //
 //   warp 8      TMA producer: the Q tile once, then K tiles (256 keys x 128 d)
 //               and V^T tiles (d x 256 keys) through a shared-memory ring

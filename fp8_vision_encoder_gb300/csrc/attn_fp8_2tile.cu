@@ -24,7 +24,7 @@
 //   S buffer per tile, and each tile's next scores are computed while its
 //   softmax works on the current ones.
 //
-//   warp 8      TMA: Q_A and Q_B once, then K tiles (128 keys x 128 bytes) and
+//   warp 8      TMA: Q_A and Q_B, then K tiles (128 keys x 128 bytes) and
 //               V^T tiles (d rows x 128 keys) through a 4-stage ring.
 //   warp 9      S issuer (one thread): S_X(j) = Q_X K_j^T, 128 x 128 per tile.
 //   warp 10     P.V issuer (one thread): O_X += P_X(j) V_j, alternating A, B.
@@ -40,6 +40,11 @@
 // two, so P' and O differ only where a weight falls in E4M3's subnormal range
 // or the fp32 rounding of the exponent argument lands differently (about 1 %
 // of outputs by one bf16 ulp on the pages' workloads).
+//
+// Two kernels run the units: attn_fp8_2tile_kernel one unit per CTA,
+// attn_fp8_2tile_persistent_kernel one CTA per SM taking units from a counter
+// (for segments of up to 6144 tokens, where a unit's fixed cost weighs most);
+// both compute every unit the same way, so their outputs are bit-identical.
 //
 // Every wait is bounded; on expiry the CTA records VITFP8_ERR_DEVICE_TIMEOUT
 // in the workspace error word, all roles leave their loops, wait (bounded)
